@@ -1,0 +1,195 @@
+"""CPU oracle for FP8 E4M3 128x128 block quantization and the block-scaled NT GEMM.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference leg of ``bench.py`` may import this package. The product
+path (``block_quantize_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``dgfp8_oracle.c`` (plain C, FP64 accumulation, IEEE
+FP32 division, no fast-math); this module compiles it with gcc and wraps it for
+numpy arrays. Every function cites the page section it follows:
+
+* lpnh.cn DeepGEMM walkthrough (untitled), §3.1 and §4.2: scale = block
+  max|x| / 448 in FP32, divide, round to nearest-even E4M3; §5.4 all-zero block.
+* pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析", §3.1: NT layout, FP32 or
+  power-of-two (UE8M0) scales; §2.3/§3.2: M-grouped GEMM for MoE experts.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dgfp8_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BLOCK = 128
+SCALE_FP32 = 0
+SCALE_UE8M0 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, IEEE arithmetic) if stale."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, f32p, u8p, f64p, i64p = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p)
+        lib.oracle_e4m3_table.argtypes = [f64p]
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode_array.argtypes = [f32p, i64, u8p]
+        lib.oracle_pow2_ceil.argtypes = [ctypes.c_float]
+        lib.oracle_pow2_ceil.restype = ctypes.c_float
+        lib.oracle_quantize.argtypes = [f32p, i64, i64, i64, ctypes.c_int, u8p, i64, f32p]
+        lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_gemm_nt_rows.argtypes = [u8p, i64, f32p, u8p, i64, f32p,
+                                            i64, i64, i64, i64p, i64, f64p, f64p]
+        lib.oracle_grouped_gemm_rows.argtypes = [u8p, i64, f32p, u8p, f32p, i64,
+                                                 ctypes.c_void_p, i64, i64, i64,
+                                                 i64p, i64, f64p, f64p]
+        lib.oracle_grouped_gemm_rows.restype = ctypes.c_int
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def e4m3_table() -> np.ndarray:
+    """The 256 E4M3 code values as float64 (NaN for 0x7F and 0xFF)."""
+    out = np.empty(256, dtype=np.float64)
+    _load().oracle_e4m3_table(_ptr(out))
+    return out
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Nearest E4M3 code (ties to even, saturating to +-448) of float32 values."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def pow2_ceil(s: float) -> float:
+    """Smallest power of two >= s, clamped to >= 2^-127 (UE8M0 scale)."""
+    return float(_load().oracle_pow2_ceil(ctypes.c_float(s)))
+
+
+def quantize(x: np.ndarray, mode: int = SCALE_FP32):
+    """128x128 block quantization of a float32 matrix.
+
+    Returns (q uint8 [rows, cols], scales float32 [ceil(rows/128), ceil(cols/128)]).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(((rows + BLOCK - 1) // BLOCK, (cols + BLOCK - 1) // BLOCK), dtype=np.float32)
+    rc = _load().oracle_quantize(_ptr(x), rows, cols, cols, int(mode), _ptr(q), cols, _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle.quantize: input holds a non-finite value")
+    return q, s
+
+
+def _rows_arg(rows, m):
+    if rows is None:
+        rows = np.arange(m, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if rows.size and (rows.min() < 0 or rows.max() >= m):
+        raise IndexError("row index out of range")
+    return rows
+
+
+def gemm_nt(qa, sa, qb, sb, rows=None, want_e: bool = True):
+    """Block-scaled NT GEMM in float64: C[r, j] for i = rows[r] and all j.
+
+    qa uint8 [M, K], sa float32 [ceil(M/128), K/128], qb uint8 [N, K],
+    sb float32 [ceil(N/128), K/128]. Returns (C, E) (E None if not wanted).
+    """
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sb = np.ascontiguousarray(sb, dtype=np.float32)
+    m, k = qa.shape
+    n, k2 = qb.shape
+    if k != k2 or k % BLOCK:
+        raise ValueError("K mismatch or not a multiple of 128")
+    if sa.shape != ((m + BLOCK - 1) // BLOCK, k // BLOCK) or \
+            sb.shape != ((n + BLOCK - 1) // BLOCK, k // BLOCK):
+        raise ValueError("scale shape mismatch")
+    rows = _rows_arg(rows, m)
+    c = np.empty((rows.size, n), dtype=np.float64)
+    e = np.empty((rows.size, n), dtype=np.float64) if want_e else None
+    _load().oracle_gemm_nt_rows(_ptr(qa), k, _ptr(sa), _ptr(qb), k, _ptr(sb), m, n, k,
+                                _ptr(rows), rows.size, _ptr(c),
+                                _ptr(e) if want_e else None)
+    return c, e
+
+
+def grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=None, want_e: bool = True):
+    """M-grouped contiguous GEMM in float64 (rows with index -1 are zero).
+
+    qa uint8 [M_tot, K], sa float32 [M_tot/128, K/128], qb uint8 [G, N, K],
+    sb float32 [G, ceil(N/128), K/128], m_indices int32 [M_tot].
+    """
+    qa = np.ascontiguousarray(qa, dtype=np.uint8)
+    qb = np.ascontiguousarray(qb, dtype=np.uint8)
+    sa = np.ascontiguousarray(sa, dtype=np.float32)
+    sb = np.ascontiguousarray(sb, dtype=np.float32)
+    mi = np.ascontiguousarray(m_indices, dtype=np.int32)
+    m_tot, k = qa.shape
+    g, n, k2 = qb.shape
+    if k != k2 or k % BLOCK or mi.shape != (m_tot,):
+        raise ValueError("shape mismatch")
+    if sb.shape != (g, (n + BLOCK - 1) // BLOCK, k // BLOCK):
+        raise ValueError("sb shape mismatch")
+    rows = _rows_arg(rows, m_tot)
+    c = np.empty((rows.size, n), dtype=np.float64)
+    e = np.empty((rows.size, n), dtype=np.float64) if want_e else None
+    rc = _load().oracle_grouped_gemm_rows(_ptr(qa), k, _ptr(sa), _ptr(qb), _ptr(sb), g,
+                                          _ptr(mi), m_tot, n, k, _ptr(rows), rows.size,
+                                          _ptr(c), _ptr(e) if want_e else None)
+    if rc != 0:
+        raise ValueError("m_indices holds an expert id >= G")
+    return c, e
+
+
+def dequantize(q, s) -> np.ndarray:
+    """float64 values dec(q) * s for each 128x128 block (a test helper)."""
+    t = e4m3_table()
+    q = np.asarray(q, dtype=np.uint8)
+    vals = t[q]
+    rows, cols = q.shape
+    expand = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), BLOCK, axis=0), BLOCK, axis=1)
+    return vals * expand[:rows, :cols]
