@@ -1,0 +1,344 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 E4M3 block-scaled GEMM path on GB300.
+
+A step is one pass of the hot path over the LLM-projection workload: for each
+of the four shapes M = 4096, (N, K) in {(7168, 2048), (2112, 7168),
+(24576, 1536), (4096, 7168)}, quantize the FP32 activation A[M, K] to E4M3 with
+128x128 FP32 block scales (dg_quantize_fp8_block), then run the block-scaled NT
+GEMM against the pre-quantized weight B[N, K] into bf16 C[M, N]
+(dg_fp8_gemm_nt). Weights are quantized once, outside the timed region, as
+weights are. Inputs are N(0,1) times a per-row log-normal magnitude, seeded.
+
+value   = GEMM FLOPs (2 M N K summed over the shapes) / device time of the step,
+          in TFLOP/s, with every input resident in HBM; the per-step working
+          set (~0.7 GB) is larger than L2, so nothing is served from a warm L2.
+e2e     = the same metric through the same C-ABI calls with host buffers: the
+          FP32 activations are copied from pinned host memory and C is copied
+          back every step, inside the timed region.
+roofline = the GEMM kernel (the dominant one), per launch: 2 M N K / its mean
+          CUDA-event duration, against the FP8 dense peak (measured bf16 cuBLAS
+          peak x 2, the nominal fp8/bf16 ratio).
+
+--impl reference times the CPU oracle (the only reference this path has) on a
+bounded sample of the same workload: the first 128 rows of every activation
+(quantize the 128-row block, GEMM those rows against all of B).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s (LLM projections M=4096, activation quantize + GEMM per step)"
+WORKLOAD = ("LLM-projection dense GEMMs, M=4096, (N,K) in {(7168,2048),(2112,7168),(24576,1536),"
+            "(4096,7168)}, bf16 out, 128x128 FP32 block scales")
+FP8_PER_BF16 = 2.0          # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1700.0
+
+
+def shapes():
+    return [(synthetic.LLM_M, n, k) for n, k in synthetic.LLM_NK]
+
+
+def step_flops():
+    return sum(2.0 * m * n * k for m, n, k in shapes())
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS,
+                "hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_sample(rows_per_shape: int, reps: int = 1):
+    """Time the CPU oracle on the first `rows_per_shape` rows of each activation."""
+    import oracle
+    oracle.build()
+    ops, secs = 0.0, 0.0
+    for idx, (m, n, k) in enumerate(shapes()):
+        rng_seed = synthetic.seed_for(2, idx)
+        b = synthetic.lognormal_rows((n, k), rng_seed + 500)
+        qb, sb = oracle.quantize(b)
+        a = synthetic.lognormal_rows((m, k), rng_seed)[:rows_per_shape]
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            qa, sa = oracle.quantize(a)
+            oracle.gemm_nt(qa, sa, qb, sb, want_e=False)
+            secs += time.perf_counter() - t0
+            ops += 2.0 * rows_per_shape * n * k
+    return ops, secs, oracle.num_threads()
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    rows = 128
+    for _ in range(args.warmup):
+        cpu_sample(rows)
+    t_ops, t_secs, cores = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        ops, secs, cores = cpu_sample(rows)
+        t_ops += ops
+        t_secs += secs
+    value = t_ops / t_secs / 1e12
+    sample = (f"first {rows} rows of each of the 4 activations (quantize one 128-row block, "
+              f"GEMM those rows against all N) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_quantize_gb300 as bq
+
+    rank, world, local = env_rank()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    bq.lib()
+
+    # Inputs: activations (FP32) and pre-quantized weights, all resident in HBM.
+    gen = torch.Generator(device=dev)
+    acts, wq, wsc, outs, qa_buf, sa_buf = [], [], [], [], [], []
+    for idx, (m, n, k) in enumerate(shapes()):
+        gen.manual_seed(synthetic.seed_for(2, idx) + 7919 * rank)
+        a = torch.randn((m, k), generator=gen, device=dev) * torch.exp(
+            torch.randn((m, 1), generator=gen, device=dev))
+        b = torch.randn((n, k), generator=gen, device=dev) * torch.exp(
+            torch.randn((n, 1), generator=gen, device=dev))
+        qb, sb = bq.dg_quantize_fp8_block(b)
+        del b
+        acts.append(a)
+        wq.append(qb)
+        wsc.append(sb)
+        qa_buf.append(torch.empty((m, k), dtype=torch.uint8, device=dev))
+        sa_buf.append(torch.empty(((m + 127) // 128, k // 128), dtype=torch.float32, device=dev))
+        outs.append(torch.empty((m, n), dtype=torch.bfloat16, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        for i in range(len(acts)):
+            bq.dg_quantize_fp8_block(acts[i], 0, qa_buf[i], sa_buf[i])
+            if events is not None:
+                events[i][0].record(stream)
+            bq.dg_fp8_gemm_nt(outs[i], qa_buf[i], wq[i], sa_buf[i], wsc[i])
+            if events is not None:
+                events[i][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+    if bq.dg_get_device_status() != bq.DG_OK:
+        raise RuntimeError("kernel timeout during warm-up")
+
+    # Device-timed region: K steps, GEMM launches bracketed by events.
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in shapes()] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    barrier()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    for s in range(args.steps):
+        step(ev[s])
+    t1.record(stream)
+    barrier()
+    clock_info = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1)
+    gemm_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(shapes()))]
+               for s in range(args.steps)]
+    status = bq.dg_get_device_status()
+    if status != bq.DG_OK:
+        raise RuntimeError(f"kernel status {bq.dg_status_string(status)}")
+
+    # End-to-end through the same calls with host buffers (pinned), copies timed.
+    host_a = [a.cpu().pin_memory() for a in acts]
+    host_c = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    dev_a = [torch.empty_like(a) for a in acts]
+
+    def e2e_step():
+        for i in range(len(acts)):
+            dev_a[i].copy_(host_a[i], non_blocking=True)
+            bq.dg_quantize_fp8_block(dev_a[i], 0, qa_buf[i], sa_buf[i])
+            bq.dg_fp8_gemm_nt(outs[i], qa_buf[i], wq[i], sa_buf[i], wsc[i])
+            host_c[i].copy_(outs[i], non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = sum(a.numel() * 4 for a in acts)
+    d2h = sum(o.numel() * 2 for o in outs)
+
+    # Max over ranks.
+    tm = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(tm[0]), float(tm[1])
+
+    if rank == 0:
+        flops = step_flops()
+        value = world * flops * args.steps / (ms * 1e-3) / 1e12
+        e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+        peaks, peak_src = measured_peaks()
+        fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+        per_shape = []
+        tot_flops, tot_ms = 0.0, 0.0
+        for i, (m, n, k) in enumerate(shapes()):
+            t = statistics.mean(gemm_ms[s][i] for s in range(args.steps))
+            per_shape.append({"M": m, "N": n, "K": k, "ms": t, "tflops": 2.0 * m * n * k / (t * 1e-3) / 1e12})
+            tot_flops += 2.0 * m * n * k
+            tot_ms += t
+        gemm_tflops = tot_flops / (tot_ms * 1e-3) / 1e12
+        ops, secs, cores = cpu_sample(256, reps=3)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3xe4m3->f32 (bf16 out)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (0.7 GB per step)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * len(shapes()) * args.steps,
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (fp8/bf16 nominal)"},
+            "cpu_baseline": {"value": ops / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": "first 256 rows of each of the 4 activations, quantize + GEMM, 3 reps"},
+            "clocks": clock_info,
+            "kernels": {"gemm_per_shape": per_shape,
+                        "quantize_ms_per_step": ms / args.steps - tot_ms},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = p.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

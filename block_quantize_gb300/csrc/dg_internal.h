@@ -1,0 +1,45 @@
+// dg_internal.h -- host-side launchers shared by the C ABI (api.cpp) and the
+// CUDA translation units. Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace dg {
+
+// 128x128 block quantizer launch (sizes already validated, rows, cols > 0).
+cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            uint8_t* q, int64_t ld_q, float* scales, bool pow2_scales,
+                            cudaStream_t stream);
+
+// One dense or M-grouped GEMM problem (sizes already validated).
+struct GemmProblem {
+  void* c;
+  int64_t ld_c;
+  const uint8_t* a;
+  int64_t ld_a;
+  const float* sa;
+  const uint8_t* b;
+  int64_t ld_b;            // dense: row stride of B; grouped: K
+  const float* sb;
+  const int32_t* m_indices;  // nullptr for the dense GEMM
+  int num_groups;            // 1 for the dense GEMM
+  int64_t M, N, K;
+  int num_sms_cap;           // 0 = every SM
+};
+
+// Returns a dg_status value.
+int launch_gemm(const GemmProblem& p, cudaStream_t stream);
+
+// Reads and clears the current device's status word (a bitmask of kernel
+// timeouts). Returns the CUDA error of the copy.
+cudaError_t read_and_clear_status(unsigned int* out);
+
+// Launches one block that waits on a barrier nothing arrives at, so that its
+// bounded wait runs out after limit_ns.
+cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+// Default limit of every in-kernel wait (1 second).
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;
+
+}  // namespace dg

@@ -1,0 +1,579 @@
+// gemm.cu -- persistent FP8 (E4M3) block-scaled NT GEMM for sm_103a, dense and
+// M-grouped contiguous.
+//
+//   C[m, n] = bf16( sum_kb sa[m/128, kb] * sb[n/128, kb] * sum_{k in kb} A[m,k] B[n,k] )
+//
+// The method: E4M3 operands with one FP32 scale per 128x128 block, partial
+// products restored with scale_a * scale_b and accumulated in FP32 (lpnh.cn
+// DeepGEMM walkthrough §2.2, §3.1, §3.2); NT layout and the
+// fp8_gemm_nt(c, a, b, a_sf, b_sf) call (pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库
+// 解析" §3.1, §4.1); grouped GEMM over MoE experts (same page §2.3, §3.2).
+//
+// Blackwell design (not the pages' Hopper pipeline):
+//   * one CTA per SM, persistent over 128 x BN output tiles in a grouped
+//     raster (16 M-blocks at a time) so the tiles in flight share A and B in L2;
+//   * warp 0 issues TMA loads of 128x128-byte A and BNx128-byte B tiles
+//     (128-byte swizzle, out-of-bounds rows zero-filled) into a ring of stages
+//     guarded by full/empty mbarriers;
+//   * warp 1 issues tcgen05.mma kind::f8f6f4 (4 x K=32 per 128-wide K block)
+//     into one of NUM_PBUF TMEM buffers, one buffer per K block, and commits to
+//     the stage's empty barrier and the buffer's full barrier;
+//   * warps 4-11 (two warpgroups, one per half of the tile's columns) read the
+//     K block's partial sums from TMEM (tcgen05.ld), release the buffer, and
+//     promote them into FP32 registers: acc += (sa * sb) * partial. After the
+//     last K block they round to bf16 and store.
+// Every mbarrier wait is bounded; on a timeout the CTA raises an abort flag,
+// records it in the device status word, drains its in-flight copies and MMAs,
+// frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "dg_device.cuh"
+#include "dg_internal.h"
+#include "../../include/dgfp8.h"
+
+namespace dg {
+
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kBM = 128;          // tile rows (tcgen05 M)
+constexpr int kBK = 128;          // K block = scale block = one 128-byte swizzle row
+constexpr int kThreads = 384;     // 3 warpgroups
+constexpr int kFirstEpiWarp = 4;  // warps 4..11 run the epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kMaxStages = 32;
+constexpr int kGroupM = 16;       // raster group height in M-blocks
+constexpr uint32_t kATileBytes = kBM * kBK;  // what one MMA reads for A
+constexpr int kSmemBudget = 200 * 1024;      // operand stages
+constexpr size_t kMinSmemPerCta = 120 * 1024;  // > half the SM's shared memory
+
+struct GemmArgs {
+  __nv_bfloat16* c;
+  int64_t ld_c;
+  const float* sa;
+  const float* sb;
+  const int32_t* m_indices;
+  int M, N;
+  int num_kb;      // K / 128
+  int num_mb;      // ceil(M / 128)
+  int num_nb;      // ceil(N / BN)
+  int nbs;         // ceil(N / 128): rows of one expert's sb
+  int num_stages;
+  uint32_t a_stage_bytes;  // smem bytes of one A stage (>= the A box, 1024-aligned)
+  uint32_t a_box_bytes;    // bytes one A TMA box delivers
+  uint64_t wait_limit_ns;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr uint32_t kBTileBytes = BN * kBK;
+  static constexpr int kNumPBuf = (512 / BN) < 8 ? (512 / BN) : 8;
+  static constexpr uint32_t kTmemCols = kNumPBuf * BN;  // power of two in [32, 512]
+  static constexpr int kCols = BN / 2;                  // columns per epilogue thread
+  static constexpr int kChunk = kCols < 32 ? kCols : 32;
+  static constexpr int kUnroll = (32 / kCols) > 1 ? ((32 / kCols) < kNumPBuf / 2 ? 32 / kCols : kNumPBuf / 2) : 1;
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M=128");
+};
+
+// Output tile of persistent iteration t: grouped raster, M fastest inside a
+// group of kGroupM M-blocks.
+__device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& mb, int& nb) {
+  const int per_group = kGroupM * num_nb;
+  const int grp = t / per_group;
+  const int first = grp * kGroupM;
+  const int gm = min(kGroupM, num_mb - first);
+  const int r = t - grp * per_group;
+  mb = first + r % gm;
+  nb = r / gm;
+}
+
+// Expert of 128-row block mb: the largest id among its rows (rows carry one id
+// or -1). Warp-collective: 32 lanes read 4 ids each.
+__device__ __forceinline__ int block_group(const int32_t* m_indices, int mb, int lane) {
+  const int4 v = __ldg(reinterpret_cast<const int4*>(m_indices + static_cast<int64_t>(mb) * kBM) + lane);
+  const int m = max(max(v.x, v.y), max(v.z, v.w));
+  return __reduce_max_sync(0xFFFFFFFFu, m);
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) break;
+  }
+}
+
+template <int BN, bool kGrouped>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = args.num_stages;
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + static_cast<size_t>(S) * args.a_stage_bytes;
+  // An MMA always reads a full 128-row A tile (16 KB) from its stage's start;
+  // rows past a short A box are junk that only feeds output rows >= M. Keep the
+  // read of the last stage inside the allocation.
+  size_t tail_off = static_cast<size_t>(S) * (args.a_stage_bytes + C::kBTileBytes);
+  const size_t a_read_end = static_cast<size_t>(S - 1) * args.a_stage_bytes + kATileBytes;
+  if (a_read_end > tail_off) tail_off = a_read_end;
+  uint8_t* smem_tail = smem + tail_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_tail);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kMaxStages;
+  uint64_t* tfull_bar = bars + 2 * kMaxStages;
+  uint64_t* tempty_bar = tfull_bar + C::kNumPBuf;
+  uint64_t* drain_bar = tempty_bar + C::kNumPBuf;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t limit = args.wait_limit_ns;
+  unsigned int* status = &g_status_word;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < C::kNumPBuf; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain_bar), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = args.num_mb * args.num_nb;
+  uint32_t loads_issued = 0;  // producer: K-block loads issued
+  bool mma_issued = false;    // MMA warp: issued at least one MMA
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, args.num_mb, args.num_nb, mb, nb);
+      int g = 0;
+      if constexpr (kGrouped) {
+        g = block_group(args.m_indices, mb, lane);
+        if (g < 0) continue;
+      }
+      for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+        const uint32_t stage = it % S;
+        const uint32_t par = (it / S) & 1u;
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&empty_bar[stage]), par ^ 1u, abort_flag, status, limit);
+          if (ok) {
+            const uint32_t fb = smem_u32(&full_bar[stage]);
+            mbar_arrive_expect_tx(fb, args.a_box_bytes + C::kBTileBytes);
+            tma_load_2d(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, mb * kBM);
+            if constexpr (kGrouped)
+              tma_load_3d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN, g);
+            else
+              tma_load_2d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN);
+            ++loads_issued;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue --
+    uint32_t it = 0, kit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, args.num_mb, args.num_nb, mb, nb);
+      if constexpr (kGrouped) {
+        if (block_group(args.m_indices, mb, lane) < 0) continue;
+      }
+      for (int kb = 0; kb < args.num_kb; ++kb, ++it, ++kit) {
+        const uint32_t stage = it % S;
+        const uint32_t par = (it / S) & 1u;
+        const uint32_t buf = kit % C::kNumPBuf;
+        const uint32_t bpar = (kit / C::kNumPBuf) & 1u;
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&tempty_bar[buf]), bpar ^ 1u, abort_flag, status, limit) &&
+               mbar_wait(smem_u32(&full_bar[stage]), par, abort_flag, status, limit);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t d = tmem_base + buf * BN;
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(smem_a + stage * args.a_stage_bytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(smem_b + stage * C::kBTileBytes));
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k) {
+              // 32 E4M3 values = 32 bytes further along the swizzled row: +2 in addr>>4.
+              mma_e4m3(d, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&empty_bar[stage]));
+            mma_commit(smem_u32(&tfull_bar[buf]));
+            mma_issued = true;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue --
+    const int ew = warp - kFirstEpiWarp;
+    const int half = ew / 4;               // which half of the tile's columns
+    const int lg = warp & 3;               // TMEM lane group this warp may access
+    const int row_in_tile = lg * 32 + lane;
+    const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16);
+    constexpr int kCols = C::kCols;
+    constexpr int kU = C::kUnroll;
+    uint32_t kit = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(t, args.num_mb, args.num_nb, mb, nb);
+      int g = 0;
+      if constexpr (kGrouped) g = block_group(args.m_indices, mb, lane);
+      const bool skip = kGrouped && g < 0;
+      const int col0 = nb * BN + half * kCols;
+      const bool half_valid = col0 < args.N;
+      const int sb_block = min(col0 / kBK, args.nbs - 1);
+      const float* sa_row = args.sa + static_cast<int64_t>(mb) * args.num_kb;
+      const float* sb_row =
+          args.sb + (static_cast<int64_t>(g) * args.nbs + sb_block) * args.num_kb;
+
+      float acc[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+
+      if (!skip) {
+        for (int kb = 0; kb < args.num_kb && ok; kb += kU) {
+          const int cnt = min(kU, args.num_kb - kb);
+          float s[kU];
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            s[u] = (u < cnt && half_valid) ? __ldg(sa_row + kb + u) * __ldg(sb_row + kb + u) : 0.f;
+          bool w = true;
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            if (u < cnt) {
+              const uint32_t buf = (kit + u) % C::kNumPBuf;
+              const uint32_t bpar = ((kit + u) / C::kNumPBuf) & 1u;
+              w = w && mbar_wait(smem_u32(&tfull_bar[buf]), bpar, abort_flag, status, limit);
+            }
+          }
+          ok = __all_sync(0xFFFFFFFFu, w);
+          if (!ok) break;
+          tc_fence_after();
+          if constexpr (kCols <= 64) {
+            uint32_t r[kU][kCols];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              if (u < cnt) {
+                const uint32_t col = ((kit + u) % C::kNumPBuf) * BN + half * kCols;
+#pragma unroll
+                for (int ch = 0; ch < kCols / C::kChunk; ++ch)
+                  tmem_ld<C::kChunk>(tmem_row + col + ch * C::kChunk, &r[u][ch * C::kChunk]);
+              }
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int u = 0; u < kU; ++u)
+                if (u < cnt) mbar_arrive(smem_u32(&tempty_bar[(kit + u) % C::kNumPBuf]));
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              if (u < cnt) {
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) acc[j] = fmaf(s[u], __uint_as_float(r[u][j]), acc[j]);
+              }
+            }
+          } else {
+            // Wide tiles (kU == 1): 32 columns at a time to bound register use.
+            const uint32_t col = (kit % C::kNumPBuf) * BN + half * kCols;
+#pragma unroll
+            for (int ch = 0; ch < kCols / 32; ++ch) {
+              uint32_t r[32];
+              tmem_ld<32>(tmem_row + col + ch * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                acc[ch * 32 + j] = fmaf(s[0], __uint_as_float(r[j]), acc[ch * 32 + j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[kit % C::kNumPBuf]));
+          }
+          kit += cnt;
+        }
+        if (!ok) break;
+      }
+
+      // Round to bf16 and store this thread's row segment.
+      const int row = mb * kBM + row_in_tile;
+      if (row < args.M && half_valid) {
+        bool zero_row = skip;
+        if constexpr (kGrouped) zero_row = zero_row || (__ldg(args.m_indices + row) < 0);
+        __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c + col0;
+#pragma unroll
+        for (int j = 0; j < kCols; j += 8) {
+          float v[8];
+#pragma unroll
+          for (int t2 = 0; t2 < 8; ++t2) v[t2] = zero_row ? 0.f : acc[j + t2];
+          if (col0 + j + 8 <= args.N) {
+            uint4 pk;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+            pk.x = *reinterpret_cast<uint32_t*>(&h0);
+            pk.y = *reinterpret_cast<uint32_t*>(&h1);
+            pk.z = *reinterpret_cast<uint32_t*>(&h2);
+            pk.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(crow + j) = pk;
+          } else {
+#pragma unroll
+            for (int t2 = 0; t2 < 8; ++t2)
+              if (col0 + j + t2 < args.N) crow[j + t2] = __float2bfloat16_rn(v[t2]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown --
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t drain_ns = 10000000ull;  // 10 ms per outstanding operation
+    if (warp == 0 && lane == 0) {
+      const uint32_t n = loads_issued < static_cast<uint32_t>(S) ? loads_issued : S;
+      for (uint32_t j = loads_issued - n; j < loads_issued; ++j)
+        drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1u, drain_ns);
+    }
+    if (warp == 1 && lane == 0 && mma_issued) {
+      mma_commit(smem_u32(drain_bar));
+      drain_wait(smem_u32(drain_bar), 0, drain_ns);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// A block whose only wait is on a barrier that nothing arrives at.
+__global__ void timeout_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, &g_status_word, limit_ns);
+  }
+  __syncthreads();
+}
+
+// --------------------------------------------------------------- host side --
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+};
+
+DeviceInfo device_info(int dev) {
+  static DeviceInfo cache[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return DeviceInfo{};
+  if (cache[dev].num_sms == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev].num_sms = n;
+  }
+  return cache[dev];
+}
+
+// Fraction of SM slots busy over the waves of a persistent launch.
+double wave_efficiency(int64_t tiles, int sms) {
+  const int64_t waves = (tiles + sms - 1) / sms;
+  return static_cast<double>(tiles) / static_cast<double>(waves * sms);
+}
+
+int pick_bn(int64_t M, int64_t N, int sms) {
+  if (M > 256) return 128;
+  // Small M streams B from HBM: pick the widest tile that keeps the SMs evenly loaded.
+  const int cands[4] = {128, 64, 32, 16};
+  int best = 16;
+  double best_eff = -1.0;
+  for (int bn : cands) {
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+    const double eff = wave_efficiency(tiles, sms);
+    if (eff >= 0.85 && tiles >= sms) return bn;
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int BN, bool kGrouped>
+int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
+  using Cf = Cfg<BN>;
+  GemmArgs args{};
+  args.c = static_cast<__nv_bfloat16*>(p.c);
+  args.ld_c = p.ld_c;
+  args.sa = p.sa;
+  args.sb = p.sb;
+  args.m_indices = p.m_indices;
+  args.M = static_cast<int>(p.M);
+  args.N = static_cast<int>(p.N);
+  args.num_kb = static_cast<int>(p.K / kBK);
+  args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
+  args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
+  args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+
+  // A box: all 128 rows, or the valid rows (multiple of 8) when M is small.
+  const uint32_t a_rows = p.M >= kBM ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
+  args.a_box_bytes = a_rows * kBK;
+  args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
+  const uint32_t stage_bytes = args.a_stage_bytes + Cf::kBTileBytes;
+  int stages = static_cast<int>(kSmemBudget / stage_bytes);
+  stages = std::min(stages, kMaxStages);
+  stages = std::min<int64_t>(stages, std::max<int64_t>(2, args.num_kb * 2));
+  stages = std::max(stages, 2);
+  args.num_stages = stages;
+
+  size_t tail_off = static_cast<size_t>(stages) * stage_bytes;
+  const size_t a_read_end = static_cast<size_t>(stages - 1) * args.a_stage_bytes + kATileBytes;
+  if (a_read_end > tail_off) tail_off = a_read_end;
+  size_t smem = 1024 + tail_off + (2 * kMaxStages + 2 * Cf::kNumPBuf + 1) * sizeof(uint64_t) + 16;
+  // One CTA per SM: the grid is persistent and each CTA owns its SM's TMEM.
+  smem = std::max<size_t>(smem, kMinSmemPerCta);
+
+  CUtensorMap ta, tb;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_a)};
+    const cuuint32_t box[2] = {kBK, a_rows};
+    if (!encode_map(&ta, p.a, 2, dims, strides, box)) return DG_ERR_CUDA;
+  }
+  if (kGrouped) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N),
+                                static_cast<cuuint64_t>(p.num_groups)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.K),
+                                   static_cast<cuuint64_t>(p.K) * static_cast<cuuint64_t>(p.N)};
+    const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(BN), 1};
+    if (!encode_map(&tb, p.b, 3, dims, strides, box)) return DG_ERR_CUDA;
+  } else {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_b)};
+    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
+    if (!encode_map(&tb, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
+  }
+
+  auto kernel = fp8_gemm_kernel<BN, kGrouped>;
+  static std::atomic<uint64_t> attr_set{0};
+  if (dev < 64 && !(attr_set.load() & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+        cudaSuccess)
+      return DG_ERR_CUDA;
+    attr_set.fetch_or(1ull << dev);
+  }
+  const int64_t tiles = static_cast<int64_t>(args.num_mb) * args.num_nb;
+  int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+  if (p.num_sms_cap > 0) grid = std::min(grid, p.num_sms_cap);
+  grid = std::max(grid, 1);
+  kernel<<<grid, kThreads, smem, stream>>>(ta, tb, args);
+  return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
+  const int sms = device_info(dev).num_sms;
+  if (sms <= 0) return DG_ERR_NO_DEVICE;
+  const int bn = pick_bn(p.M, p.N, sms);
+  const bool grouped = p.m_indices != nullptr;
+  switch (bn) {
+    case 16: return grouped ? run_gemm<16, true>(p, stream, dev, sms) : run_gemm<16, false>(p, stream, dev, sms);
+    case 32: return grouped ? run_gemm<32, true>(p, stream, dev, sms) : run_gemm<32, false>(p, stream, dev, sms);
+    case 64: return grouped ? run_gemm<64, true>(p, stream, dev, sms) : run_gemm<64, false>(p, stream, dev, sms);
+    default: return grouped ? run_gemm<128, true>(p, stream, dev, sms) : run_gemm<128, false>(p, stream, dev, sms);
+  }
+}
+
+cudaError_t read_and_clear_status(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status_word, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(unsigned int));
+}
+
+cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,147 @@
+/*
+ * dgfp8.h -- C ABI of the GB300 (sm_103a) FP8 E4M3 block-scaled GEMM library.
+ *
+ * The library computes, on one GPU:
+ *   1. 128x128 block quantization of an FP32 matrix to E4M3 codes plus one
+ *      scale per block (scale = block max|x| / 448, FP32, or rounded up to a
+ *      power of two), as the lpnh.cn DeepGEMM walkthrough describes in §3.1 and
+ *      §4.2 (steps 1-5, round to nearest even) and §5.4 (all-zero blocks);
+ *   2. the NT GEMM  C[M,N] (bf16) = sum over 128-wide K blocks kb of
+ *      sa[m/128,kb] * sb[n/128,kb] * (A_kb . B_kb^T), with A[M,K] and B[N,K]
+ *      E4M3 codes stored K-contiguous, FP32 accumulation (walkthrough §2.2 and
+ *      §3.2; pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析" §3.1 NT layout and
+ *      §4.1 fp8_gemm_nt(c, a, b, a_sf, b_sf));
+ *   3. the M-grouped contiguous variant for MoE experts, where each 128-row
+ *      block of A belongs to one expert whose B and scales it uses (pzsr.cn
+ *      page §2.3, §3.2, §3.3).
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer that the caller allocated and owns;
+ *     the library allocates no device memory per call and keeps no pointer.
+ *   - Matrices are row-major. `ld_*` is the row stride in ELEMENTS.
+ *   - Scale arrays are row-major FP32, one value per 128x128 block, with
+ *     ceil-division at ragged edges: sa is [ceil(M/128)][K/128],
+ *     sb is [ceil(N/128)][K/128], quantizer scales are
+ *     [ceil(rows/128)][ceil(cols/128)]. Their row stride is their width.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every compute
+ *     call is asynchronous on it; argument errors are reported synchronously
+ *     and launch nothing.
+ *   - Return value: a dg_status. No C++ exception crosses this boundary.
+ *   - Timeouts: every wait inside a kernel is bounded; a wait that runs out sets
+ *     a per-device status word and makes the kernel return early (its output is
+ *     then undefined). dg_get_device_status() reads and clears that word.
+ */
+#ifndef DGFP8_H_
+#define DGFP8_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define DG_API __declspec(dllexport)
+#else
+#define DG_API __attribute__((visibility("default")))
+#endif
+
+#define DG_ABI_VERSION 1u
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad mode or stride */
+    DG_ERR_UNSUPPORTED_SHAPE = 2,  /* K not a multiple of 128, M_tot not a multiple of 128, dim >= 2^31 */
+    DG_ERR_MISALIGNED = 3,         /* pointer or stride breaks a 16-byte (TMA) rule */
+    DG_ERR_CUDA = 4,               /* a CUDA runtime call or a launch failed */
+    DG_ERR_NO_DEVICE = 5,          /* no CUDA device, or the device is not sm_103 */
+    DG_ERR_TIMEOUT = 6             /* a bounded in-kernel wait ran out (see above) */
+} dg_status;
+
+typedef enum {
+    DG_SCALE_FP32 = 0,   /* scale = fl32(max|x| / 448); 1.0 for an all-zero block */
+    DG_SCALE_UE8M0 = 1   /* the FP32 scale rounded up to a power of two, >= 2^-127 */
+} dg_scale_mode;
+
+/* ABI version of the loaded library (DG_ABI_VERSION at build time). */
+DG_API uint32_t dg_get_abi_version(void);
+
+/* Static English text for a status code (never NULL). */
+DG_API const char *dg_status_string(int status);
+
+/* Row alignment that the M-grouped contiguous layout needs: every expert's
+ * rows start on a multiple of this (128). pzsr.cn page §3.3 names the query
+ * get_mk_alignment_for_contiguous_layout(). */
+DG_API int dg_get_mk_alignment_for_contiguous_layout(void);
+
+/* Cap the number of SMs the GEMM's persistent grid uses (0 = all SMs), the
+ * DG_SET_NUM_SMS knob of pzsr.cn page §3.3. Applies to later calls from every
+ * thread. Returns DG_ERR_INVALID_ARG for n < 0. */
+DG_API int dg_set_num_sms(int n);
+
+/* The current cap (0 = all SMs). */
+DG_API int dg_get_num_sms(void);
+
+/* Block quantizer (walkthrough §4.2 steps 1-5, §3.1, §5.4).
+ *   x       [rows][ld_x] FP32, finite values (NaN/Inf give unspecified codes)
+ *   q       [rows][ld_q] E4M3 codes out: RNE of fl32(x / s), saturated to +-448,
+ *           the sign of zero kept
+ *   scales  [ceil(rows/128)][ceil(cols/128)] FP32 out
+ *   scale_mode  a dg_scale_mode
+ * rows == 0 or cols == 0 is a no-op. Needs ld_x >= cols and ld_q >= cols.
+ * Any alignment works; 16-byte aligned x with ld_x % 4 == 0, and q with
+ * ld_q % 4 == 0, take the vectorized path. */
+DG_API int dg_quantize_fp8_block(const float *x, int64_t rows, int64_t cols, int64_t ld_x,
+                                 uint8_t *q, int64_t ld_q, float *scales,
+                                 int scale_mode, void *stream);
+
+/* Dense NT GEMM (walkthrough §2.2, §3.2; pzsr.cn page §3.1, §4.1).
+ *   c   [M][ld_c] bf16 out (raw 16-bit storage), rounded to nearest even
+ *   a   [M][ld_a] E4M3 codes, K contiguous;  sa [ceil(M/128)][K/128] FP32
+ *   b   [N][ld_b] E4M3 codes, K contiguous;  sb [ceil(N/128)][K/128] FP32
+ *   scale_mode  DG_SCALE_UE8M0 promises that every scale is a power of two
+ *               (it is not checked); DG_SCALE_FP32 accepts any finite scale.
+ * Needs K % 128 == 0, ld_a >= K, ld_b >= K, ld_c >= N; a, b and c 16-byte
+ * aligned, ld_a and ld_b multiples of 16, ld_c a multiple of 8; sa, sb 4-byte
+ * aligned. M == 0 or N == 0 is a no-op; K == 0 writes zeros. */
+DG_API int dg_fp8_gemm_nt(void *c, int64_t ld_c,
+                          const uint8_t *a, int64_t ld_a, const float *sa,
+                          const uint8_t *b, int64_t ld_b, const float *sb,
+                          int64_t M, int64_t N, int64_t K,
+                          int scale_mode, void *stream);
+
+/* M-grouped contiguous GEMM for MoE experts (pzsr.cn page §2.3, §3.2, §3.3).
+ *   c          [M_tot][ld_c] bf16 out
+ *   a          [M_tot][ld_a] E4M3 codes; sa [M_tot/128][K/128] FP32
+ *   b          [num_groups][N][K] E4M3 codes, packed (row stride K)
+ *   sb         [num_groups][ceil(N/128)][K/128] FP32
+ *   m_indices  [M_tot] int32 on the device: the expert of each row, or -1 for a
+ *              padding row. Rows of one 128-row block carry one expert id or -1
+ *              (each expert's rows start on a multiple of 128). Output rows with
+ *              -1 are written as zeros; a block made only of -1 rows is zero.
+ *              Ids >= num_groups make that block's result undefined.
+ * Needs M_tot % 128 == 0 and the alignment rules of dg_fp8_gemm_nt (with
+ * ld_b = K). */
+DG_API int dg_fp8_grouped_gemm_contiguous(void *c, int64_t ld_c,
+                                          const uint8_t *a, int64_t ld_a, const float *sa,
+                                          const uint8_t *b, const float *sb, int num_groups,
+                                          const int32_t *m_indices,
+                                          int64_t M_tot, int64_t N, int64_t K,
+                                          int scale_mode, void *stream);
+
+/* Synchronize `stream`, then read and clear the current device's status word.
+ * Returns DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
+ * call, DG_ERR_CUDA if the stream reports an error, else DG_OK. */
+DG_API int dg_get_device_status(void *stream);
+
+/* Self-test of the timeout path: launches one block whose wait on a barrier
+ * that nothing arrives at runs out after `limit_ns` nanoseconds (clamped to
+ * [1e3, 1e9]); the block then records the timeout and returns. Follow with
+ * dg_get_device_status(), which must report DG_ERR_TIMEOUT. */
+DG_API int dg_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGFP8_H_ */

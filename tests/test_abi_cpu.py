@@ -1,0 +1,105 @@
+"""CPU checks of the C-ABI library: it loads, exports every entry point that
+include/dgfp8.h declares, and rejects bad arguments before touching CUDA (so
+these run without a GPU). Calls with valid arguments on a machine without a GPU
+return DG_ERR_NO_DEVICE and launch nothing."""
+import ctypes
+
+import pytest
+import torch
+
+import block_quantize_gb300 as bq
+from block_quantize_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return bq.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = bq.declared_functions()
+    assert {"dg_quantize_fp8_block", "dg_fp8_gemm_nt", "dg_fp8_grouped_gemm_contiguous"} <= set(names)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_version_strings_alignment(L):
+    assert bq.dg_get_abi_version() == 1
+    assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
+    for s in range(7):
+        assert bq.dg_status_string(s)
+    assert bq.dg_status_string(99) == "unknown status"
+
+
+def test_num_sms_knob(L):
+    assert bq.dg_get_num_sms() == 0
+    bq.dg_set_num_sms(64)
+    assert bq.dg_get_num_sms() == 64
+    with pytest.raises(bq.DgError):
+        bq.dg_set_num_sms(-1)
+    bq.dg_set_num_sms(0)
+
+
+P = 1 << 20        # fake, 1 MiB-aligned device addresses: never dereferenced
+NULL = None
+
+
+def gemm(L, c=P, ldc=256, a=P, lda=512, sa=P, b=P, ldb=512, sb=P, m=128, n=256, k=512, mode=0):
+    return L.dg_fp8_gemm_nt(c, ldc, a, lda, sa, b, ldb, sb, m, n, k, mode, None)
+
+
+def grouped(L, c=P, ldc=256, a=P, lda=512, sa=P, b=P, sb=P, g=2, mi=P, m=256, n=256, k=512, mode=0):
+    return L.dg_fp8_grouped_gemm_contiguous(c, ldc, a, lda, sa, b, sb, g, mi, m, n, k, mode, None)
+
+
+def quant(L, x=P, rows=128, cols=128, ldx=128, q=P, ldq=128, s=P, mode=0):
+    return L.dg_quantize_fp8_block(x, rows, cols, ldx, q, ldq, s, mode, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(c=NULL), bq.DG_ERR_INVALID_ARG), (dict(a=NULL), bq.DG_ERR_INVALID_ARG),
+    (dict(sb=NULL), bq.DG_ERR_INVALID_ARG), (dict(m=-1), bq.DG_ERR_INVALID_ARG),
+    (dict(mode=7), bq.DG_ERR_INVALID_ARG), (dict(lda=256), bq.DG_ERR_INVALID_ARG),
+    (dict(ldc=100), bq.DG_ERR_INVALID_ARG),
+    (dict(k=500, lda=512, ldb=512), bq.DG_ERR_UNSUPPORTED_SHAPE),
+    (dict(m=1 << 31), bq.DG_ERR_UNSUPPORTED_SHAPE),
+    (dict(a=P + 8), bq.DG_ERR_MISALIGNED), (dict(c=P + 2), bq.DG_ERR_MISALIGNED),
+    (dict(lda=520), bq.DG_ERR_MISALIGNED), (dict(ldc=260), bq.DG_ERR_MISALIGNED),
+    (dict(m=0), bq.DG_OK), (dict(n=0), bq.DG_OK),
+])
+def test_gemm_argument_errors(L, kw, status):
+    assert gemm(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(mi=NULL), bq.DG_ERR_INVALID_ARG), (dict(g=0), bq.DG_ERR_INVALID_ARG),
+    (dict(m=200), bq.DG_ERR_UNSUPPORTED_SHAPE), (dict(mi=P + 4), bq.DG_ERR_MISALIGNED),
+    (dict(k=384 + 64), bq.DG_ERR_UNSUPPORTED_SHAPE), (dict(m=0), bq.DG_OK),
+])
+def test_grouped_argument_errors(L, kw, status):
+    assert grouped(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=NULL), bq.DG_ERR_INVALID_ARG), (dict(s=NULL), bq.DG_ERR_INVALID_ARG),
+    (dict(rows=-1), bq.DG_ERR_INVALID_ARG), (dict(ldx=100), bq.DG_ERR_INVALID_ARG),
+    (dict(ldq=100), bq.DG_ERR_INVALID_ARG), (dict(mode=2), bq.DG_ERR_INVALID_ARG),
+    (dict(x=P + 2), bq.DG_ERR_MISALIGNED), (dict(rows=0), bq.DG_OK), (dict(cols=0), bq.DG_OK),
+])
+def test_quantize_argument_errors(L, kw, status):
+    assert quant(L, **kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_arguments_without_gpu_report_no_device(L):
+    assert gemm(L) == bq.DG_ERR_NO_DEVICE
+    assert grouped(L) == bq.DG_ERR_NO_DEVICE
+    assert quant(L) == bq.DG_ERR_NO_DEVICE
+    assert L.dg_selftest_wait_timeout(1000, None) == bq.DG_ERR_NO_DEVICE
+
+
+def test_python_binding_rejects_cpu_tensors(L):
+    x = torch.zeros(4, 4)
+    with pytest.raises(ValueError):
+        bq.dg_quantize_fp8_block(x)

@@ -1,0 +1,96 @@
+"""GPU parity of the M-grouped contiguous GEMM (MoE experts) against the CPU
+oracle, through the C ABI (pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析" §2.3,
+§3.2, §3.3: grouped GEMM along M, rows aligned to
+get_mk_alignment_for_contiguous_layout()). Operands come from the oracle's
+quantizer; padding rows (index -1) must come out as zeros."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantize_gb300 as bq
+import synthetic
+from parity import assert_within_bound, device, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _quantize_experts(oracle_mod, b, mode=0):
+    qs, ss = zip(*[oracle_mod.quantize(b[g], mode) for g in range(b.shape[0])])
+    return np.stack(qs), np.stack(ss)
+
+
+def _run(qa, sa, qb, sb, m_idx, mode=0):
+    dev = device()
+    m_tot, n = qa.shape[0], qb.shape[1]
+    c = torch.full((m_tot, n), float("nan"), dtype=torch.bfloat16, device=dev)
+    bq.dg_fp8_grouped_gemm_contiguous(c, to_dev(qa, dev), to_dev(qb, dev), to_dev(sa, dev),
+                                      to_dev(sb, dev), to_dev(m_idx, dev), mode)
+    assert bq.dg_get_device_status() == bq.DG_OK
+    return c
+
+
+def _rows_per_group(m_idx, per_group, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for g in np.unique(m_idx):
+        idx = np.flatnonzero(m_idx == g)
+        rows.append(idx[[0, -1]])
+        rows.append(rng.choice(idx, size=min(per_group, idx.size), replace=False))
+    return np.unique(np.concatenate(rows)).astype(np.int64)
+
+
+def test_alignment_query():
+    device()
+    assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_small_groups_with_empty_expert_and_padding(oracle_mod, mode):
+    k, n, g = 384, 200, 4
+    sizes = np.array([5, 0, 130, 128])
+    m_idx, offs = synthetic.moe_layout(sizes)
+    m_idx = np.concatenate([m_idx, np.full(128, -1, np.int32)])   # one block of pure padding
+    a = synthetic.lognormal_rows((m_idx.size, k), seed=201)
+    b = synthetic.lognormal_rows((g * n, k), seed=202).reshape(g, n, k)
+    qa, sa = oracle_mod.quantize(a, mode)
+    qa[m_idx < 0] = 0x7F                       # NaN codes in padding rows must not leak
+    qb, sb = _quantize_experts(oracle_mod, b, mode)
+    c = _run(qa, sa, qb, sb, m_idx, mode)
+    ref, mag = oracle_mod.grouped_gemm_contiguous(qa, sa, qb, sb, m_idx)
+    assert_within_bound(c, ref, mag, "small grouped")
+    assert torch.count_nonzero(c[torch.as_tensor(m_idx < 0, device=c.device)]) == 0
+
+
+def test_moe_config(oracle_mod):
+    """8 experts, K = 4096 hidden, N = 11008 intermediate, 4096 tokens top-2."""
+    mo = synthetic.MOE
+    a, b, m_idx, sizes = synthetic.moe_inputs(seed=0, experts=mo["experts"], tokens=mo["tokens"],
+                                               topk=mo["topk"], hidden=mo["hidden"],
+                                               intermediate=mo["intermediate"])
+    assert m_idx.size == 8960 and list(sizes) == [1033, 1551, 36, 6, 873, 2462, 1027, 1204]
+    qa, sa = oracle_mod.quantize(a)
+    qb, sb = _quantize_experts(oracle_mod, b)
+    c = _run(qa, sa, qb, sb, m_idx)
+    rows = _rows_per_group(m_idx, 6, seed=1)
+    ref, mag = oracle_mod.grouped_gemm_contiguous(qa, sa, qb, sb, m_idx, rows=rows)
+    assert_within_bound(c[torch.as_tensor(rows, device=c.device)], ref, mag, "MoE 8x11008x4096")
+
+
+def test_grouped_matches_dense_bitwise(oracle_mod):
+    """A grouped call with one expert per 128-row block equals the dense calls on
+    each expert's rows, bit for bit."""
+    k, n = 256, 384
+    sizes = np.array([128, 256])
+    m_idx, offs = synthetic.moe_layout(sizes)
+    a = synthetic.normal((m_idx.size, k), seed=203)
+    b = synthetic.normal((2 * n, k), seed=204).reshape(2, n, k)
+    qa, sa = oracle_mod.quantize(a)
+    qb, sb = _quantize_experts(oracle_mod, b)
+    c = _run(qa, sa, qb, sb, m_idx)
+    dev = device()
+    for g in range(2):
+        lo, hi = offs[g], offs[g + 1]
+        cd = torch.empty((hi - lo, n), dtype=torch.bfloat16, device=dev)
+        bq.dg_fp8_gemm_nt(cd, to_dev(qa[lo:hi], dev), to_dev(qb[g], dev),
+                          to_dev(sa[lo // 128:hi // 128], dev), to_dev(sb[g], dev))
+        assert torch.equal(cd.view(torch.int16), c[lo:hi].view(torch.int16))
