@@ -195,7 +195,7 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: F32 accumulator
 // (bits 4-5 = 1), A and B E4M3 (bits 7-9, 10-12 = 0), both K-major
 // (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

@@ -47,9 +47,7 @@ namespace {
 
 constexpr int kBM = 128;          // tile rows (tcgen05 M)
 constexpr int kBK = 128;          // K block = scale block = one 128-byte swizzle row
-constexpr int kThreads = 384;     // 3 warpgroups
-constexpr int kFirstEpiWarp = 4;  // warps 4..11 run the epilogue
-constexpr int kEpiWarps = 8;
+constexpr int kFirstEpiWarp = 4;  // the epilogue warpgroups start at warp 4
 constexpr int kMaxStages = 32;
 constexpr int kGroupM = 16;       // raster group height in M-blocks
 constexpr uint32_t kATileBytes = kBM * kBK;  // what one MMA reads for A
@@ -75,15 +73,28 @@ struct GemmArgs {
 
 template <int BN>
 struct Cfg {
+  // Wide tiles use four epilogue warpgroups (64 accumulator registers per thread).
+  static constexpr int kEpiWG = (BN == 256) ? 4 : 2;
+  static constexpr int kThreads = 128 * (1 + kEpiWG);
+  static constexpr int kEpiWarps = 4 * kEpiWG;
+  // Warps 1..kIssuers take turns issuing the MMAs of successive K blocks: one
+  // thread needs ~70 cycles per tcgen05.mma and ~150 per mbarrier wait, more than
+  // a 128-wide tile's 256 MMA cycles per K block, so the issue work is spread.
+  static constexpr int kIssuers = (BN >= 256) ? 2 : 3;
   static constexpr uint32_t kBTileBytes = BN * kBK;
   static constexpr int kNumPBuf = (512 / BN) < 8 ? (512 / BN) : 8;
   static constexpr uint32_t kTmemCols = kNumPBuf * BN;  // power of two in [32, 512]
-  static constexpr int kCols = BN / 2;                  // columns per epilogue thread
-  static constexpr int kChunk = kCols < 32 ? kCols : 32;
-  static constexpr int kUnroll = (32 / kCols) > 1 ? ((32 / kCols) < kNumPBuf / 2 ? 32 / kCols : kNumPBuf / 2) : 1;
+  static constexpr int kCols = BN / kEpiWG;             // columns per epilogue thread
+  // Columns per tcgen05.ld; 16 on wide tiles keeps 640 threads within 96 registers.
+  static constexpr int kChunk = (BN == 256) ? 16 : (kCols < 32 ? kCols : 32);
+  static constexpr int kBatch = (BN == 256) ? 1 : (kCols / kChunk);  // loads before one wait
+  static constexpr int kUnroll =
+      (32 / kCols) > 1 ? ((32 / kCols) < kNumPBuf / 2 ? 32 / kCols : kNumPBuf / 2) : 1;
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M=128");
+  static_assert(kIssuers <= 3, "issuers live in warps 1..3");
+  static_assert(kCols % (kChunk * kBatch) == 0, "epilogue batching");
 };
 
 // Output tile of persistent iteration t: grouped raster, M fastest inside a
@@ -115,7 +126,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 }
 
 template <int BN, bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
   using C = Cfg<BN>;
@@ -154,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < C::kNumPBuf; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
-      mbar_init(smem_u32(&tempty_bar[b]), kEpiWarps);
+      mbar_init(smem_u32(&tempty_bar[b]), C::kEpiWarps);
     }
-    mbar_init(smem_u32(drain_bar), 1);
+    mbar_init(smem_u32(drain_bar), C::kIssuers);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
@@ -170,7 +181,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int num_tiles = args.num_mb * args.num_nb;
   uint32_t loads_issued = 0;  // producer: K-block loads issued
-  bool mma_issued = false;    // MMA warp: issued at least one MMA
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -205,9 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp >= 1 && warp <= C::kIssuers) {
     // ----------------------------------------------------------- MMA issue --
-    uint32_t it = 0, kit = 0;
+    // This warp issues K blocks it with it % kIssuers == warp - 1; K block it
+    // accumulates into TMEM buffer it % kNumPBuf.
+    const uint32_t me = static_cast<uint32_t>(warp - 1);
+    uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       int mb, nb;
@@ -215,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kGrouped) {
         if (block_group(args.m_indices, mb, lane) < 0) continue;
       }
-      for (int kb = 0; kb < args.num_kb; ++kb, ++it, ++kit) {
+      for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+        if (it % C::kIssuers != me) continue;
         const uint32_t stage = it % S;
         const uint32_t par = (it / S) & 1u;
-        const uint32_t buf = kit % C::kNumPBuf;
-        const uint32_t bpar = (kit / C::kNumPBuf) & 1u;
+        const uint32_t buf = it % C::kNumPBuf;
+        const uint32_t bpar = (it / C::kNumPBuf) & 1u;
         if (lane == 0) {
           ok = mbar_wait(smem_u32(&tempty_bar[buf]), bpar ^ 1u, abort_flag, status, limit) &&
                mbar_wait(smem_u32(&full_bar[stage]), par, abort_flag, status, limit);
@@ -235,7 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(smem_u32(&empty_bar[stage]));
             mma_commit(smem_u32(&tfull_bar[buf]));
-            mma_issued = true;
           }
         }
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
@@ -246,13 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue --
     const int ew = warp - kFirstEpiWarp;
-    const int half = ew / 4;               // which half of the tile's columns
+    const int part = ew / 4;               // which slice of the tile's columns
     const int lg = warp & 3;               // TMEM lane group this warp may access
     const int row_in_tile = lg * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16);
     constexpr int kCols = C::kCols;
     constexpr int kU = C::kUnroll;
-    uint32_t kit = 0;
+    constexpr int kPer = C::kChunk * C::kBatch;  // columns per load-wait round
+    uint32_t it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       int mb, nb;
@@ -260,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       if constexpr (kGrouped) g = block_group(args.m_indices, mb, lane);
       const bool skip = kGrouped && g < 0;
-      const int col0 = nb * BN + half * kCols;
-      const bool half_valid = col0 < args.N;
+      const int col0 = nb * BN + part * kCols;
+      const bool part_valid = col0 < args.N;
       const int sb_block = min(col0 / kBK, args.nbs - 1);
       const float* sa_row = args.sa + static_cast<int64_t>(mb) * args.num_kb;
       const float* sb_row =
@@ -277,28 +291,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s[kU];
 #pragma unroll
           for (int u = 0; u < kU; ++u)
-            s[u] = (u < cnt && half_valid) ? __ldg(sa_row + kb + u) * __ldg(sb_row + kb + u) : 0.f;
+            s[u] = (u < cnt && part_valid) ? __ldg(sa_row + kb + u) * __ldg(sb_row + kb + u) : 0.f;
           bool w = true;
 #pragma unroll
           for (int u = 0; u < kU; ++u) {
             if (u < cnt) {
-              const uint32_t buf = (kit + u) % C::kNumPBuf;
-              const uint32_t bpar = ((kit + u) / C::kNumPBuf) & 1u;
+              const uint32_t buf = (it + u) % C::kNumPBuf;
+              const uint32_t bpar = ((it + u) / C::kNumPBuf) & 1u;
               w = w && mbar_wait(smem_u32(&tfull_bar[buf]), bpar, abort_flag, status, limit);
             }
           }
           ok = __all_sync(0xFFFFFFFFu, w);
           if (!ok) break;
           tc_fence_after();
-          if constexpr (kCols <= 64) {
+          if constexpr (kU > 1) {
+            // Narrow tiles: the partials of kU K blocks at once.
             uint32_t r[kU][kCols];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
               if (u < cnt) {
-                const uint32_t col = ((kit + u) % C::kNumPBuf) * BN + half * kCols;
-#pragma unroll
-                for (int ch = 0; ch < kCols / C::kChunk; ++ch)
-                  tmem_ld<C::kChunk>(tmem_row + col + ch * C::kChunk, &r[u][ch * C::kChunk]);
+                const uint32_t col = ((it + u) % C::kNumPBuf) * BN + part * kCols;
+                tmem_ld<kCols>(tmem_row + col, &r[u][0]);
               }
             }
             tmem_wait_ld();
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
 #pragma unroll
               for (int u = 0; u < kU; ++u)
-                if (u < cnt) mbar_arrive(smem_u32(&tempty_bar[(kit + u) % C::kNumPBuf]));
+                if (u < cnt) mbar_arrive(smem_u32(&tempty_bar[(it + u) % C::kNumPBuf]));
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -317,29 +330,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            // Wide tiles (kU == 1): 32 columns at a time to bound register use.
-            const uint32_t col = (kit % C::kNumPBuf) * BN + half * kCols;
+            // kPer columns per round (one wait::ld per round) to bound registers.
+            const uint32_t col = (it % C::kNumPBuf) * BN + part * kCols;
 #pragma unroll
-            for (int ch = 0; ch < kCols / 32; ++ch) {
-              uint32_t r[32];
-              tmem_ld<32>(tmem_row + col + ch * 32, r);
+            for (int rd = 0; rd < kCols / kPer; ++rd) {
+              uint32_t r[kPer];
+#pragma unroll
+              for (int b = 0; b < C::kBatch; ++b)
+                tmem_ld<C::kChunk>(tmem_row + col + rd * kPer + b * C::kChunk, &r[b * C::kChunk]);
               tmem_wait_ld();
+              if (rd == kCols / kPer - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[it % C::kNumPBuf]));
+              }
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                acc[ch * 32 + j] = fmaf(s[0], __uint_as_float(r[j]), acc[ch * 32 + j]);
+              for (int j = 0; j < kPer; ++j)
+                acc[rd * kPer + j] = fmaf(s[0], __uint_as_float(r[j]), acc[rd * kPer + j]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[kit % C::kNumPBuf]));
           }
-          kit += cnt;
+          it += cnt;
         }
         if (!ok) break;
       }
 
       // Round to bf16 and store this thread's row segment.
       const int row = mb * kBM + row_in_tile;
-      if (row < args.M && half_valid) {
+      if (row < args.M && part_valid) {
         bool zero_row = skip;
         if constexpr (kGrouped) zero_row = zero_row || (__ldg(args.m_indices + row) < 0);
         __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c + col0;
@@ -379,10 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t j = loads_issued - n; j < loads_issued; ++j)
         drain_wait(smem_u32(&full_bar[j % S]), (j / S) & 1u, drain_ns);
     }
-    if (warp == 1 && lane == 0 && mma_issued) {
-      mma_commit(smem_u32(drain_bar));
-      drain_wait(smem_u32(drain_bar), 0, drain_ns);
-    }
+    // Every issuer commits once: the barrier completes when all their MMAs are done.
+    if (warp >= 1 && warp <= C::kIssuers && lane == 0) mma_commit(smem_u32(drain_bar));
+    if (warp == 1 && lane == 0) drain_wait(smem_u32(drain_bar), 0, drain_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -458,7 +474,7 @@ double wave_efficiency(int64_t tiles, int sms) {
 }
 
 int pick_bn(int64_t M, int64_t N, int sms) {
-  if (M > 256) return 128;
+  if (M > 256) return 256;
   // Small M streams B from HBM: pick the widest tile that keeps the SMs evenly loaded.
   const int cands[4] = {128, 64, 32, 16};
   int best = 16;
@@ -543,7 +559,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   if (p.num_sms_cap > 0) grid = std::min(grid, p.num_sms_cap);
   grid = std::max(grid, 1);
-  kernel<<<grid, kThreads, smem, stream>>>(ta, tb, args);
+  kernel<<<grid, Cf::kThreads, smem, stream>>>(ta, tb, args);
   return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
@@ -560,7 +576,8 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
     case 16: return grouped ? run_gemm<16, true>(p, stream, dev, sms) : run_gemm<16, false>(p, stream, dev, sms);
     case 32: return grouped ? run_gemm<32, true>(p, stream, dev, sms) : run_gemm<32, false>(p, stream, dev, sms);
     case 64: return grouped ? run_gemm<64, true>(p, stream, dev, sms) : run_gemm<64, false>(p, stream, dev, sms);
-    default: return grouped ? run_gemm<128, true>(p, stream, dev, sms) : run_gemm<128, false>(p, stream, dev, sms);
+    case 128: return grouped ? run_gemm<128, true>(p, stream, dev, sms) : run_gemm<128, false>(p, stream, dev, sms);
+    default: return grouped ? run_gemm<256, true>(p, stream, dev, sms) : run_gemm<256, false>(p, stream, dev, sms);
   }
 }
 
