@@ -2,6 +2,7 @@
 // CUDA translation units. Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -38,6 +39,19 @@ cudaError_t read_and_clear_status(unsigned int* out);
 // Launches one block that waits on a barrier nothing arrives at, so that its
 // bounded wait runs out after limit_ns.
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (128-byte
+// swizzle or none); false if the driver call is unavailable or rejects the map.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                       const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                       bool swizzle128);
+
+// Device address of the current device's status word (resolved once per device
+// with cudaGetSymbolAddress); nullptr on failure.
+unsigned int* device_status_word();
+
+// Number of SMs of device `dev` (0 if unknown).
+int device_sm_count(int dev);
 
 // Default limit of every in-kernel wait (1 second).
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;

@@ -15,13 +15,17 @@
 //   * warp 0 issues TMA loads of 128x128-byte A and BNx128-byte B tiles
 //     (128-byte swizzle, out-of-bounds rows zero-filled) into a ring of stages
 //     guarded by full/empty mbarriers;
-//   * warp 1 issues tcgen05.mma kind::f8f6f4 (4 x K=32 per 128-wide K block)
-//     into one of NUM_PBUF TMEM buffers, one buffer per K block, and commits to
-//     the stage's empty barrier and the buffer's full barrier;
-//   * warps 4-11 (two warpgroups, one per half of the tile's columns) read the
-//     K block's partial sums from TMEM (tcgen05.ld), release the buffer, and
-//     promote them into FP32 registers: acc += (sa * sb) * partial. After the
-//     last K block they round to bf16 and store.
+//   * warps 1..kIssuers take turns, one K block each, issuing the four
+//     tcgen05.mma kind::f8f6f4 (K = 32 each) of a K block into its own TMEM
+//     buffer, then committing to the stage's empty barrier and the buffer's
+//     full barrier. One issuing thread needs ~70 cycles per MMA and ~150 per
+//     mbarrier wait (measured on GB300), more than a K block's MMA time, so the
+//     issue work is spread over several warps;
+//   * the epilogue warpgroups (one per column slice) read each K block's
+//     partial sums from TMEM (tcgen05.ld), release the buffer and promote them
+//     in FP32 registers: acc += (sa * sb) * partial. After the last K block each
+//     warp rounds its 32 x 64 box to bf16 into 128-byte-swizzled shared memory
+//     and writes it with a TMA store (clipped at the M and N edges).
 // Every mbarrier wait is bounded; on a timeout the CTA raises an abort flag,
 // records it in the device status word, drains its in-flight copies and MMAs,
 // frees its TMEM and returns.
@@ -33,6 +37,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "dg_device.cuh"
@@ -47,12 +52,12 @@ namespace {
 
 constexpr int kBM = 128;          // tile rows (tcgen05 M)
 constexpr int kBK = 128;          // K block = scale block = one 128-byte swizzle row
-constexpr int kFirstEpiWarp = 4;  // the epilogue warpgroups start at warp 4
 constexpr int kMaxStages = 32;
 constexpr int kGroupM = 16;       // raster group height in M-blocks
-constexpr uint32_t kATileBytes = kBM * kBK;  // what one MMA reads for A
-constexpr int kSmemBudget = 200 * 1024;      // operand stages
+constexpr uint32_t kATileBytes = kBM * kBK;    // what one MMA reads for A
 constexpr size_t kMinSmemPerCta = 120 * 1024;  // > half the SM's shared memory
+constexpr size_t kMaxDynSmem = 227 * 1024;
+constexpr uint32_t kWarpOutBytes = 32 * 32 * 2;  // one warp's 32 x 32 bf16 output box
 
 struct GemmArgs {
   __nv_bfloat16* c;
@@ -73,28 +78,36 @@ struct GemmArgs {
 
 template <int BN>
 struct Cfg {
-  // Wide tiles use four epilogue warpgroups (64 accumulator registers per thread).
+  // Wide tiles: four epilogue warpgroups, 64 columns and accumulators each.
   static constexpr int kEpiWG = (BN == 256) ? 4 : 2;
-  static constexpr int kThreads = 128 * (1 + kEpiWG);
+  // Warps 1 and 2 take turns issuing the MMAs of successive K blocks. With an
+  // even number of TMEM buffers and of stages, issuer i only ever touches the
+  // buffers and stages with index parity i, so each barrier has one waiter
+  // that sees its phases in order (a parity wait cannot tell phase n from n-2).
+  static constexpr int kIssuers = 2;
+  static constexpr int kFirstEpiWarp = 1 + kIssuers;  // warp 0 produces
   static constexpr int kEpiWarps = 4 * kEpiWG;
-  // Warps 1..kIssuers take turns issuing the MMAs of successive K blocks: one
-  // thread needs ~70 cycles per tcgen05.mma and ~150 per mbarrier wait, more than
-  // a 128-wide tile's 256 MMA cycles per K block, so the issue work is spread.
-  static constexpr int kIssuers = (BN >= 256) ? 2 : 3;
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr uint32_t kBTileBytes = BN * kBK;
   static constexpr int kNumPBuf = (512 / BN) < 8 ? (512 / BN) : 8;
   static constexpr uint32_t kTmemCols = kNumPBuf * BN;  // power of two in [32, 512]
   static constexpr int kCols = BN / kEpiWG;             // columns per epilogue thread
-  // Columns per tcgen05.ld; 16 on wide tiles keeps 640 threads within 96 registers.
+  // Columns per tcgen05.ld: 16 on wide tiles, whose 19 warps leave 96 registers a thread.
   static constexpr int kChunk = (BN == 256) ? 16 : (kCols < 32 ? kCols : 32);
-  static constexpr int kBatch = (BN == 256) ? 1 : (kCols / kChunk);  // loads before one wait
+  static constexpr int kBatch = (BN == 256) ? 1 : (kCols / kChunk);  // loads per wait
   static constexpr int kUnroll =
       (32 / kCols) > 1 ? ((32 / kCols) < kNumPBuf / 2 ? 32 / kCols : kNumPBuf / 2) : 1;
+  // 64-column slices leave through shared memory and TMA (each warp stages its
+  // 32 x 64 slice as two 32 x 32 boxes in turn); narrow tiles (small M) store
+  // straight from registers.
+  static constexpr bool kTmaStore = (kCols == 64);
+  static constexpr uint32_t kOutBytes = kTmaStore ? kEpiWarps * kWarpOutBytes : 0;
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 N for M=128");
-  static_assert(kIssuers <= 3, "issuers live in warps 1..3");
   static_assert(kCols % (kChunk * kBatch) == 0, "epilogue batching");
+  static_assert(kThreads <= 1024, "CTA size");
+  static_assert(kNumPBuf % kIssuers == 0, "buffer ownership by issuer");
 };
 
 // Output tile of persistent iteration t: grouped raster, M fastest inside a
@@ -125,10 +138,16 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 template <int BN, bool kGrouped>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms.
@@ -143,8 +162,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   size_t tail_off = static_cast<size_t>(S) * (args.a_stage_bytes + C::kBTileBytes);
   const size_t a_read_end = static_cast<size_t>(S - 1) * args.a_stage_bytes + kATileBytes;
   if (a_read_end > tail_off) tail_off = a_read_end;
-  uint8_t* smem_tail = smem + tail_off;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_tail);
+  uint8_t* smem_out = smem + tail_off;  // kEpiWarps boxes of kWarpOutBytes (kTmaStore)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + C::kOutBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kMaxStages;
   uint64_t* tfull_bar = bars + 2 * kMaxStages;
@@ -172,6 +191,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
+    if (C::kTmaStore) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
@@ -215,7 +235,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 1 && warp <= C::kIssuers) {
+  } else if (warp <= C::kIssuers) {
     // ----------------------------------------------------------- MMA issue --
     // This warp issues K blocks it with it % kIssuers == warp - 1; K block it
     // accumulates into TMEM buffer it % kNumPBuf.
@@ -235,6 +255,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         const uint32_t buf = it % C::kNumPBuf;
         const uint32_t bpar = (it / C::kNumPBuf) & 1u;
         if (lane == 0) {
+          // The buffer's previous use has been read by every epilogue warp, and
+          // the stage's operands have landed.
           ok = mbar_wait(smem_u32(&tempty_bar[buf]), bpar ^ 1u, abort_flag, status, limit) &&
                mbar_wait(smem_u32(&full_bar[stage]), par, abort_flag, status, limit);
           if (ok) {
@@ -256,18 +278,21 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= kFirstEpiWarp) {
+  } else {
     // ------------------------------------------------------------ epilogue --
-    const int ew = warp - kFirstEpiWarp;
+    const int ew = warp - C::kFirstEpiWarp;
     const int part = ew / 4;               // which slice of the tile's columns
-    const int lg = warp & 3;               // TMEM lane group this warp may access
+    const int lg = warp & 3;               // TMEM lane quadrant this warp may access
     const int row_in_tile = lg * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16);
     constexpr int kCols = C::kCols;
     constexpr int kU = C::kUnroll;
     constexpr int kPer = C::kChunk * C::kBatch;  // columns per load-wait round
+    uint8_t* out_box = smem_out + ew * kWarpOutBytes;  // this warp's 32 x 64 bf16 box
+    bool stores_issued = false;
     uint32_t it = 0;
     bool ok = true;
+    bool ready = false;  // the full barrier of K block `it` is known complete
     for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
@@ -281,9 +306,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const float* sb_row =
           args.sb + (static_cast<int64_t>(g) * args.nbs + sb_block) * args.num_kb;
 
-      float acc[kCols];
+      // FP32 accumulators, two columns per 64-bit register (f32x2 FMA).
+      uint64_t acc[kCols / 2];
 #pragma unroll
-      for (int j = 0; j < kCols; ++j) acc[j] = 0.f;
+      for (int j = 0; j < kCols / 2; ++j) acc[j] = 0ull;
 
       if (!skip) {
         for (int kb = 0; kb < args.num_kb && ok; kb += kU) {
@@ -295,7 +321,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           bool w = true;
 #pragma unroll
           for (int u = 0; u < kU; ++u) {
-            if (u < cnt) {
+            if (u < cnt && !(u == 0 && ready)) {
               const uint32_t buf = (it + u) % C::kNumPBuf;
               const uint32_t bpar = ((it + u) / C::kNumPBuf) & 1u;
               w = w && mbar_wait(smem_u32(&tfull_bar[buf]), bpar, abort_flag, status, limit);
@@ -322,11 +348,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
               for (int u = 0; u < kU; ++u)
                 if (u < cnt) mbar_arrive(smem_u32(&tempty_bar[(it + u) % C::kNumPBuf]));
             }
+            ready = false;
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
               if (u < cnt) {
+                const uint64_t s2 = f32x2(__float_as_uint(s[u]), __float_as_uint(s[u]));
 #pragma unroll
-                for (int j = 0; j < kCols; ++j) acc[j] = fmaf(s[u], __uint_as_float(r[u][j]), acc[j]);
+                for (int j = 0; j < kCols / 2; ++j) ffma2(acc[j], s2, f32x2(r[u][2 * j], r[u][2 * j + 1]));
               }
             }
           } else {
@@ -336,17 +364,22 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             for (int rd = 0; rd < kCols / kPer; ++rd) {
               uint32_t r[kPer];
 #pragma unroll
-              for (int b = 0; b < C::kBatch; ++b)
-                tmem_ld<C::kChunk>(tmem_row + col + rd * kPer + b * C::kChunk, &r[b * C::kChunk]);
+              for (int b2 = 0; b2 < C::kBatch; ++b2)
+                tmem_ld<C::kChunk>(tmem_row + col + rd * kPer + b2 * C::kChunk, &r[b2 * C::kChunk]);
               tmem_wait_ld();
               if (rd == kCols / kPer - 1) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[it % C::kNumPBuf]));
+                // Test the next K block's buffer now: the test's latency hides
+                // behind the multiply-adds below.
+                const uint32_t nx = it + 1;
+                ready = mbar_test(smem_u32(&tfull_bar[nx % C::kNumPBuf]), (nx / C::kNumPBuf) & 1u);
               }
+              const uint64_t s2 = f32x2(__float_as_uint(s[0]), __float_as_uint(s[0]));
 #pragma unroll
-              for (int j = 0; j < kPer; ++j)
-                acc[rd * kPer + j] = fmaf(s[0], __uint_as_float(r[j]), acc[rd * kPer + j]);
+              for (int j = 0; j < kPer / 2; ++j)
+                ffma2(acc[(rd * kPer) / 2 + j], s2, f32x2(r[2 * j], r[2 * j + 1]));
             }
           }
           it += cnt;
@@ -354,36 +387,70 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         if (!ok) break;
       }
 
-      // Round to bf16 and store this thread's row segment.
       const int row = mb * kBM + row_in_tile;
-      if (row < args.M && part_valid) {
-        bool zero_row = skip;
-        if constexpr (kGrouped) zero_row = zero_row || (__ldg(args.m_indices + row) < 0);
-        __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c + col0;
+      bool zero_row = skip;
+      if constexpr (kGrouped) zero_row = zero_row || (row < args.M && __ldg(args.m_indices + row) < 0);
+      if constexpr (C::kTmaStore) {
+        // bf16 row segment -> this warp's 64-byte-swizzled 32 x 32 box (16-byte
+        // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA store at
+        // (col0 + 32 h, mb*128 + lg*32), clipped at M and N; the two halves
+        // of the slice share the box in turn. Only this warp touches it.
+        const int row0 = mb * kBM + lg * 32;
 #pragma unroll
-        for (int j = 0; j < kCols; j += 8) {
-          float v[8];
+        for (int h = 0; h < 2; ++h) {
+          if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
+          __syncwarp();
+          uint8_t* my_row = out_box + lane * 64;
 #pragma unroll
-          for (int t2 = 0; t2 < 8; ++t2) v[t2] = zero_row ? 0.f : acc[j + t2];
-          if (col0 + j + 8 <= args.N) {
+          for (int c = 0; c < 4; ++c) {
             uint4 pk;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
-            pk.x = *reinterpret_cast<uint32_t*>(&h0);
-            pk.y = *reinterpret_cast<uint32_t*>(&h1);
-            pk.z = *reinterpret_cast<uint32_t*>(&h2);
-            pk.w = *reinterpret_cast<uint32_t*>(&h3);
-            *reinterpret_cast<uint4*>(crow + j) = pk;
-          } else {
+            const uint64_t* a2 = &acc[h * 16 + c * 4];
+            const float2 v0 = f32x2_split(a2[0]), v1 = f32x2_split(a2[1]);
+            const float2 v2 = f32x2_split(a2[2]), v3 = f32x2_split(a2[3]);
+            pk.x = zero_row ? 0u : pack_bf16x2(v0.x, v0.y);
+            pk.y = zero_row ? 0u : pack_bf16x2(v1.x, v1.y);
+            pk.z = zero_row ? 0u : pack_bf16x2(v2.x, v2.y);
+            pk.w = zero_row ? 0u : pack_bf16x2(v3.x, v3.y);
+            *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && part_valid && row0 < args.M && col0 + 32 * h < args.N) {
+            tma_store_2d(&tmap_c, smem_u32(out_box), col0 + 32 * h, row0);
+            bulk_commit();
+            stores_issued = true;
+          }
+        }
+      } else {
+        // Narrow tiles: store this thread's row segment directly.
+        if (row < args.M && part_valid) {
+          __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c + col0;
 #pragma unroll
-            for (int t2 = 0; t2 < 8; ++t2)
-              if (col0 + j + t2 < args.N) crow[j + t2] = __float2bfloat16_rn(v[t2]);
+          for (int j = 0; j < kCols; j += 8) {
+            float v[8];
+#pragma unroll
+            for (int t2 = 0; t2 < 8; t2 += 2) {
+              const float2 pr = f32x2_split(acc[(j + t2) / 2]);
+              v[t2] = zero_row ? 0.f : pr.x;
+              v[t2 + 1] = zero_row ? 0.f : pr.y;
+            }
+            if (col0 + j + 8 <= args.N) {
+              uint4 pk;
+              pk.x = pack_bf16x2(v[0], v[1]);
+              pk.y = pack_bf16x2(v[2], v[3]);
+              pk.z = pack_bf16x2(v[4], v[5]);
+              pk.w = pack_bf16x2(v[6], v[7]);
+              *reinterpret_cast<uint4*>(crow + j) = pk;
+            } else {
+#pragma unroll
+              for (int t2 = 0; t2 < 8; ++t2)
+                if (col0 + j + t2 < args.N) crow[j + t2] = __float2bfloat16_rn(v[t2]);
+            }
           }
         }
       }
     }
+    if (C::kTmaStore && lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
   }
 
@@ -439,14 +506,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                const cuuint64_t* strides, const cuuint32_t* box) {
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -473,7 +541,18 @@ double wave_efficiency(int64_t tiles, int sms) {
   return static_cast<double>(tiles) / static_cast<double>(waves * sms);
 }
 
+// Tile width override for tuning: DG_GEMM_BLOCK_N in {16, 32, 64, 128, 256}.
+int block_n_override() {
+  static const int v = [] {
+    const char* e = std::getenv("DG_GEMM_BLOCK_N");
+    const int n = e ? std::atoi(e) : 0;
+    return (n == 16 || n == 32 || n == 64 || n == 128 || n == 256) ? n : 0;
+  }();
+  return v;
+}
+
 int pick_bn(int64_t M, int64_t N, int sms) {
+  if (block_n_override()) return block_n_override();
   if (M > 256) return 256;
   // Small M streams B from HBM: pick the widest tile that keeps the SMs evenly loaded.
   const int cands[4] = {128, 64, 32, 16};
@@ -513,25 +592,32 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   args.a_box_bytes = a_rows * kBK;
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
   const uint32_t stage_bytes = args.a_stage_bytes + Cf::kBTileBytes;
-  int stages = static_cast<int>(kSmemBudget / stage_bytes);
-  stages = std::min(stages, kMaxStages);
-  stages = std::min<int64_t>(stages, std::max<int64_t>(2, args.num_kb * 2));
-  stages = std::max(stages, 2);
+  const size_t bar_bytes = (2 * kMaxStages + 2 * Cf::kNumPBuf + 1) * sizeof(uint64_t) + 16;
+  const size_t budget = kMaxDynSmem - 1024 - Cf::kOutBytes - bar_bytes;
+  // The operand ring, including the padding a short A box needs (see the kernel).
+  auto ring_bytes = [&](int st) {
+    return std::max<size_t>(static_cast<size_t>(st) * stage_bytes,
+                            static_cast<size_t>(st - 1) * args.a_stage_bytes + kATileBytes);
+  };
+  int stages = std::min<int>(kMaxStages, static_cast<int>(budget / stage_bytes));
+  stages = std::min<int64_t>(stages, std::max<int64_t>(6, args.num_kb * 2));
+  while (stages > 2 && ring_bytes(stages) > budget) --stages;
+  // Stage s must only ever be waited on by issuer s % kIssuers (see Cfg):
+  // a multiple of kIssuers stages.
+  stages = stages / Cf::kIssuers * Cf::kIssuers;
+  if (stages < Cf::kIssuers || ring_bytes(stages) > budget) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_stages = stages;
-
-  size_t tail_off = static_cast<size_t>(stages) * stage_bytes;
-  const size_t a_read_end = static_cast<size_t>(stages - 1) * args.a_stage_bytes + kATileBytes;
-  if (a_read_end > tail_off) tail_off = a_read_end;
-  size_t smem = 1024 + tail_off + (2 * kMaxStages + 2 * Cf::kNumPBuf + 1) * sizeof(uint64_t) + 16;
+  size_t smem = 1024 + ring_bytes(stages) + Cf::kOutBytes + bar_bytes;
   // One CTA per SM: the grid is persistent and each CTA owns its SM's TMEM.
   smem = std::max<size_t>(smem, kMinSmemPerCta);
+  if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_a)};
     const cuuint32_t box[2] = {kBK, a_rows};
-    if (!encode_map(&ta, p.a, 2, dims, strides, box)) return DG_ERR_CUDA;
+    if (!encode_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box)) return DG_ERR_CUDA;
   }
   if (kGrouped) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N),
@@ -539,19 +625,30 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(p.K),
                                    static_cast<cuuint64_t>(p.K) * static_cast<cuuint64_t>(p.N)};
     const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(BN), 1};
-    if (!encode_map(&tb, p.b, 3, dims, strides, box)) return DG_ERR_CUDA;
+    if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, dims, strides, box)) return DG_ERR_CUDA;
   } else {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_b)};
     const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
-    if (!encode_map(&tb, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
+    if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
+  }
+  if (Cf::kTmaStore) {
+    // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_c) * 2};
+    const cuuint32_t box[2] = {32, 32};
+    if (!encode_map(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.c, 2, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
+  } else {
+    tc = ta;  // not read by narrow tiles
   }
 
   auto kernel = fp8_gemm_kernel<BN, kGrouped>;
   static std::atomic<uint64_t> attr_set{0};
   if (dev < 64 && !(attr_set.load() & (1ull << dev))) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kMaxDynSmem)) != cudaSuccess)
       return DG_ERR_CUDA;
     attr_set.fetch_or(1ull << dev);
   }
@@ -559,11 +656,47 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   if (p.num_sms_cap > 0) grid = std::min(grid, p.num_sms_cap);
   grid = std::max(grid, 1);
-  kernel<<<grid, Cf::kThreads, smem, stream>>>(ta, tb, args);
+  kernel<<<grid, Cf::kThreads, smem, stream>>>(ta, tb, tc, args);
   return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
 }  // namespace
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                       const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                       bool swizzle128) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, st, b, e,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count(int dev) { return device_info(dev).num_sms; }
+
+unsigned int* device_status_word() {
+  static unsigned int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
 
 int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   int dev = 0;

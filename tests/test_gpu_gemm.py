@@ -142,6 +142,25 @@ def test_num_sms_cap_is_bit_identical(oracle_mod):
     assert torch.equal(full.view(torch.int16), capped.view(torch.int16))
 
 
+@pytest.mark.parametrize("cap", [1, 2, 5])
+@pytest.mark.parametrize("mnk", [(1024, 2048, 1024), (640, 1000, 384), (200, 3000, 640)])
+def test_many_tiles_per_cta(oracle_mod, cap, mnk):
+    """Few SMs -> each persistent CTA runs many tiles, so every pipeline buffer
+    and barrier goes through many phases (catches phase-aliasing races)."""
+    m, n, k = mnk
+    qa, sa, qb, sb = _operands(oracle_mod, m, n, k, seed=12 + cap, dist="lognormal")
+    full, _ = _run(qa, sa, qb, sb)
+    try:
+        bq.dg_set_num_sms(cap)
+        capped, _ = _run(qa, sa, qb, sb)
+    finally:
+        bq.dg_set_num_sms(0)
+    rows = sample_rows(m, 16, seed=cap)
+    ref, mag = oracle_mod.gemm_nt(qa, sa, qb, sb, rows=rows)
+    assert_within_bound(capped[torch.as_tensor(rows, device=capped.device)], ref, mag, f"cap {cap}")
+    assert torch.equal(full.view(torch.int16), capped.view(torch.int16))
+
+
 def test_empty_and_zero_k():
     dev = device()
     a = torch.zeros((0, 128), dtype=torch.uint8, device=dev)

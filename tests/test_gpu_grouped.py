@@ -76,6 +76,24 @@ def test_moe_config(oracle_mod):
     assert_within_bound(c[torch.as_tensor(rows, device=c.device)], ref, mag, "MoE 8x11008x4096")
 
 
+def test_grouped_few_sms(oracle_mod):
+    """Grouped GEMM with many tiles per persistent CTA."""
+    k, n, g = 512, 640, 3
+    sizes = np.array([300, 5, 640])
+    m_idx, _ = synthetic.moe_layout(sizes)
+    a = synthetic.lognormal_rows((m_idx.size, k), seed=205)
+    b = synthetic.lognormal_rows((g * n, k), seed=206).reshape(g, n, k)
+    qa, sa = oracle_mod.quantize(a)
+    qb, sb = _quantize_experts(oracle_mod, b)
+    try:
+        bq.dg_set_num_sms(2)
+        c = _run(qa, sa, qb, sb, m_idx)
+    finally:
+        bq.dg_set_num_sms(0)
+    ref, mag = oracle_mod.grouped_gemm_contiguous(qa, sa, qb, sb, m_idx)
+    assert_within_bound(c, ref, mag, "grouped, 2 SMs")
+
+
 def test_grouped_matches_dense_bitwise(oracle_mod):
     """A grouped call with one expert per 128-row block equals the dense calls on
     each expert's rows, bit for bit."""
