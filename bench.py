@@ -62,6 +62,16 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -280,11 +290,7 @@ def run_ours(args):
     h2d = sum(a.numel() * 4 for a in acts)
     d2h = sum(o.numel() * 2 for o in outs)
 
-    # Max over ranks.
-    tm = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(tm[0]), float(tm[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, dev)
 
     if rank == 0:
         flops = step_flops()
