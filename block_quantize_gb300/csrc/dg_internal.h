@@ -32,6 +32,10 @@ struct GemmProblem {
 // Returns a dg_status value.
 int launch_gemm(const GemmProblem& p, cudaStream_t stream);
 
+// Dense GEMMs with M <= 128 use the cluster split-K kernel (gemm_smallm.cu).
+bool small_m_supported(int64_t M, const void* m_indices);
+int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream);
+
 // Reads and clears the current device's status word (a bitmask of kernel
 // timeouts). Returns the CUDA error of the copy.
 cudaError_t read_and_clear_status(unsigned int* out);

@@ -703,6 +703,7 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
   const int sms = device_info(dev).num_sms;
   if (sms <= 0) return DG_ERR_NO_DEVICE;
+  if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
   const int bn = pick_bn(p.M, p.N, sms);
   const bool grouped = p.m_indices != nullptr;
   switch (bn) {

@@ -1,0 +1,557 @@
+// gemm_smallm.cu -- block-scaled NT GEMM for small M (M <= 128, decode shapes).
+//
+// Same arithmetic as gemm.cu (lpnh.cn DeepGEMM walkthrough §2.2, §3.2; pzsr.cn
+// "DeepGEMM: GPU上的高效BLAS内核库解析" §3.1, §4.1): per 128-wide K block the
+// partial products are restored with sa*sb and accumulated in FP32. With few
+// rows the work is streaming B from HBM, so the kernel is shaped for bytes in
+// flight on as many SMs as possible:
+//   * a thread-block cluster of `split` CTAs shares one BN-column tile of C
+//     (BN = 256 when M <= 64, else 128); CTA r of the cluster streams B over
+//     its own contiguous K range through a deep TMA ring, issues the MMAs and
+//     promotes the partials in registers exactly like the large-M kernel.
+//     TMA boxes of 128-byte rows stream at ~40 GB/s per SM and, over all SMs,
+//     at ~4.8 TB/s with 128-row boxes and ~5.4 TB/s with 256-row boxes
+//     (measured on GB300), hence wide tiles and a split of K over the SMs;
+//   * the cluster then reduces its `split` FP32 partial tiles through
+//     distributed shared memory: every CTA parks its partial in its own shared
+//     memory and signals every peer's `ready` mbarrier; CTA r sums the peers'
+//     values for its share of the columns in rank order (deterministic), rounds
+//     to bf16 and stores; then it signals every peer's `consumed` mbarrier so
+//     the partial buffers can be reused for the next tile;
+//   * clusters are persistent over the N tiles.
+// All waits are bounded (see dg_device.cuh). The only unbounded synchronisation
+// is the cluster-wide barrier at kernel start (peers' barriers initialised
+// before any remote arrive) and at kernel end (no CTA leaves while a peer may
+// still read its shared memory), both executed unconditionally by every thread.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/dgfp8.h"
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;
+constexpr int kMaxStages = 32;
+constexpr uint32_t kATileBytes = kBM * kBK;
+constexpr size_t kMaxDynSmem = 227 * 1024;
+constexpr size_t kMinSmemPerCta = 120 * 1024;
+constexpr int kMaxSplit = 8;
+
+template <int BN>
+struct SCfg {
+  // TMEM: 512 columns of buffers, one buffer per issuer (each issuer owns the
+  // buffer and the stages congruent to its index, so every mbarrier has one
+  // in-order waiter).
+  static constexpr int kNumPBuf = 512 / BN;
+  static constexpr int kIssuers = kNumPBuf;
+  static constexpr int kFirstEpiWarp = 1 + kIssuers;
+  static constexpr int kGroups = BN / 64;           // 64-column groups per tile
+  static constexpr int kEpiWarps = 4 * kGroups;     // x 4 lane quadrants
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+  static constexpr uint32_t kBTileBytes = BN * kBK;
+  static constexpr int kPartStride = BN + 4;        // +16 B: conflict-free row writes
+  // Columns per tcgen05.ld: 16 when 19 warps leave 96 registers per thread.
+  static constexpr int kChunk = (kThreads > 512) ? 16 : 32;
+  static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
+  static_assert(kThreads <= 1024, "CTA size");
+};
+
+struct SmallArgs {
+  __nv_bfloat16* c;
+  int64_t ld_c;
+  const float* sa;
+  const float* sb;
+  unsigned int* status;
+  int M, N;
+  int num_kb, num_nb, nbs;
+  int split;          // cluster size = number of K ranges
+  int num_clusters;   // persistent clusters (grid = num_clusters * split)
+  int num_stages;
+  int m_pad;          // partial rows kept (multiple of 32, >= M)
+  uint32_t a_stage_bytes, a_box_bytes;
+  uint64_t wait_limit_ns;
+};
+
+// Eight consecutive outputs at column gcol as bf16 (a 16-byte store when all
+// eight are inside the matrix, else element by element up to N).
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, int gcol, int N, float2 a, float2 b,
+                                             float2 c, float2 d) {
+  if (gcol + 8 <= N) {
+    uint4 pk;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(b.x, b.y);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(c.x, c.y);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(d.x, d.y);
+    pk.x = *reinterpret_cast<uint32_t*>(&h0);
+    pk.y = *reinterpret_cast<uint32_t*>(&h1);
+    pk.z = *reinterpret_cast<uint32_t*>(&h2);
+    pk.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(dst) = pk;
+  } else {
+    const float v[8] = {a.x, a.y, b.x, b.y, c.x, c.y, d.x, d.y};
+    for (int q = 0; q < 8; ++q)
+      if (gcol + q < N) dst[q] = __float2bfloat16_rn(v[q]);
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
+    fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                           const __grid_constant__ CUtensorMap tmap_b, const SmallArgs args) {
+  using C = SCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = args.num_stages;
+  uint8_t* smem_a = smem;
+  uint8_t* smem_b = smem + static_cast<size_t>(S) * args.a_stage_bytes;
+  size_t off = static_cast<size_t>(S) * (args.a_stage_bytes + C::kBTileBytes);
+  const size_t a_read_end = static_cast<size_t>(S - 1) * args.a_stage_bytes + kATileBytes;
+  if (a_read_end > off) off = a_read_end;  // an MMA reads 128 A rows from its stage
+  float* part = reinterpret_cast<float*>(smem + off);
+  off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  off = (off + 7) & ~static_cast<size_t>(7);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + kMaxStages;
+  uint64_t* tfull_bar = bars + 2 * kMaxStages;
+  uint64_t* tempty_bar = tfull_bar + C::kNumPBuf;
+  uint64_t* ready_bar = tempty_bar + C::kNumPBuf;  // all partials of the tile are parked
+  uint64_t* consumed_bar = ready_bar + 1;          // every peer has read this CTA's partial
+  uint64_t* drain_bar = consumed_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t limit = args.wait_limit_ns;
+  unsigned int* status = args.status;
+  const uint32_t rank = cluster_ctarank();
+  const int split = args.split;
+  const int cluster_id = blockIdx.x / split;
+  const int kb_lo = static_cast<int>(rank) * args.num_kb / split;
+  const int kb_hi = (static_cast<int>(rank) + 1) * args.num_kb / split;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < C::kNumPBuf; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), C::kEpiWarps);
+    }
+    mbar_init(smem_u32(ready_bar), split * C::kEpiWarps);
+    mbar_init(smem_u32(consumed_bar), split * C::kEpiWarps);
+    mbar_init(smem_u32(drain_bar), C::kIssuers);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();  // every peer's barriers exist before any remote arrive
+  const uint32_t tmem_base = *tmem_slot;
+  uint32_t loads_issued = 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    uint32_t it = 0;
+    bool ok = true;
+    for (int nb = cluster_id; nb < args.num_nb && ok; nb += args.num_clusters) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        const uint32_t stage = it % S;
+        const uint32_t par = (it / S) & 1u;
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&empty_bar[stage]), par ^ 1u, abort_flag, status, limit);
+          if (ok) {
+            const uint32_t fb = smem_u32(&full_bar[stage]);
+            mbar_arrive_expect_tx(fb, args.a_box_bytes + C::kBTileBytes);
+            tma_load_2d(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, 0);
+            tma_load_2d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN);
+            ++loads_issued;
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp <= C::kIssuers) {
+    // ----------------------------------------------------------- MMA issue --
+    const uint32_t me = static_cast<uint32_t>(warp - 1);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int nb = cluster_id; nb < args.num_nb && ok; nb += args.num_clusters) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
+        if (it % C::kIssuers != me) continue;
+        const uint32_t stage = it % S;
+        const uint32_t par = (it / S) & 1u;
+        const uint32_t buf = it % C::kNumPBuf;
+        const uint32_t bpar = (it / C::kNumPBuf) & 1u;
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&tempty_bar[buf]), bpar ^ 1u, abort_flag, status, limit) &&
+               mbar_wait(smem_u32(&full_bar[stage]), par, abort_flag, status, limit);
+          if (ok) {
+            tc_fence_after();
+            const uint64_t adesc = sw128_kmajor_desc(smem_u32(smem_a + stage * args.a_stage_bytes));
+            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(smem_b + stage * C::kBTileBytes));
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k)
+              mma_e4m3(tmem_base + buf * BN, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&empty_bar[stage]));
+            mma_commit(smem_u32(&tfull_bar[buf]));
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= C::kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue --
+    const int ew = warp - C::kFirstEpiWarp;
+    const int grp = ew >> 2;              // columns [64 grp, 64 grp + 64) of the tile
+    const int lg = warp & 3;              // TMEM lane quadrant this warp may access
+    const int row = lg * 32 + lane;
+    const bool rows_here = lg * 32 < args.M;  // this warp holds at least one real row
+    const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(lg * 32) << 16) + grp * 64;
+    // Columns this CTA reduces: an 8-column-aligned share of the tile.
+    const int col_lo = (static_cast<int>(rank) * (BN / 8) / split) * 8;
+    const int col_hi = ((static_cast<int>(rank) + 1) * (BN / 8) / split) * 8;
+    const int groups8 = (col_hi - col_lo) / 8;
+    const int work = args.M * groups8;
+    uint32_t it = 0;
+    uint32_t tile_seq = 0;
+    bool ok = true;
+    for (int nb = cluster_id; nb < args.num_nb && ok; nb += args.num_clusters, ++tile_seq) {
+      const int colt = nb * BN + grp * 64;
+      const bool valid = colt < args.N;
+      const float* sb_row = args.sb + static_cast<int64_t>(min(colt / kBK, args.nbs - 1)) * args.num_kb;
+      uint64_t acc[32];  // 64 FP32 accumulators, two per register pair
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = 0ull;
+      for (int kb = kb_lo; kb < kb_hi && ok; ++kb, ++it) {
+        const float sv = valid ? __ldg(args.sa + kb) * __ldg(sb_row + kb) : 0.f;
+        const uint32_t buf = it % C::kNumPBuf;
+        const bool w = mbar_wait(smem_u32(&tfull_bar[buf]), (it / C::kNumPBuf) & 1u, abort_flag, status, limit);
+        ok = __all_sync(0xFFFFFFFFu, w);
+        if (!ok) break;
+        tc_fence_after();
+        if (rows_here) {
+          const uint64_t s2 = f32x2(__float_as_uint(sv), __float_as_uint(sv));
+#pragma unroll
+          for (int rd = 0; rd < 64 / C::kChunk; ++rd) {
+            uint32_t r[C::kChunk];
+            tmem_ld<C::kChunk>(tmem_row + buf * BN + rd * C::kChunk, r);
+            tmem_wait_ld();
+            if (rd == 64 / C::kChunk - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+            }
+#pragma unroll
+            for (int j = 0; j < C::kChunk / 2; ++j)
+              ffma2(acc[rd * (C::kChunk / 2) + j], s2, f32x2(r[2 * j], r[2 * j + 1]));
+          }
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[buf]));
+        }
+      }
+      if (!ok) break;
+
+      if (split == 1) {
+        // No peers: round this thread's row segment to bf16 and store it.
+        if (row < args.M && valid) {
+          __nv_bfloat16* dst = args.c + static_cast<int64_t>(row) * args.ld_c + colt;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 v0 = f32x2_split(acc[4 * j]), v1 = f32x2_split(acc[4 * j + 1]);
+            const float2 v2 = f32x2_split(acc[4 * j + 2]), v3 = f32x2_split(acc[4 * j + 3]);
+            store_bf16x8(dst + 8 * j, colt + 8 * j, args.N, v0, v1, v2, v3);
+          }
+        }
+        continue;
+      }
+
+      // Park this CTA's partial (rows < M) once every peer has read the last one.
+      if (tile_seq > 0) {
+        const bool w = mbar_wait_cluster(smem_u32(consumed_bar), (tile_seq - 1) & 1u, abort_flag, status, limit);
+        ok = __all_sync(0xFFFFFFFFu, w);
+        if (!ok) break;
+      }
+      if (row < args.M) {
+        float* prow = part + row * C::kPartStride + grp * 64;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 lo = f32x2_split(acc[2 * j]), hi = f32x2_split(acc[2 * j + 1]);
+          reinterpret_cast<float4*>(prow)[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+      // The warp's writes are ordered before lane 0's releasing remote arrives.
+      __syncwarp();
+      if (lane == 0)
+        for (int s = 0; s < split; ++s) mbar_arrive_remote(mapa_shared(smem_u32(ready_bar), s));
+
+      // Reduce this CTA's columns over the cluster's partials, in rank order.
+      {
+        const bool w = mbar_wait_cluster(smem_u32(ready_bar), tile_seq & 1u, abort_flag, status, limit);
+        ok = __all_sync(0xFFFFFFFFu, w);
+        if (!ok) break;
+      }
+      for (int g = ew * 32 + lane; g < work; g += C::kEpiWarps * 32) {
+        const int rr = g / groups8;
+        const int col = col_lo + (g % groups8) * 8;
+        float sum[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum[q] = 0.f;
+        const uint32_t local = smem_u32(part + rr * C::kPartStride + col);
+        for (int s = 0; s < split; ++s) {
+          const uint32_t ra = mapa_shared(local, s);
+          const float4 x0 = ld_dsmem_f4(ra), x1 = ld_dsmem_f4(ra + 16);
+          sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
+          sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
+        }
+        const int gcol = nb * BN + col;
+        store_bf16x8(args.c + static_cast<int64_t>(rr) * args.ld_c + gcol, gcol, args.N,
+                     make_float2(sum[0], sum[1]), make_float2(sum[2], sum[3]),
+                     make_float2(sum[4], sum[5]), make_float2(sum[6], sum[7]));
+      }
+      __syncwarp();
+      if (lane == 0)
+        for (int s = 0; s < split; ++s) mbar_arrive_remote(mapa_shared(smem_u32(consumed_bar), s));
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown --
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t drain_ns = 10000000ull;
+    if (warp == 0 && lane == 0) {
+      const uint32_t n = loads_issued < static_cast<uint32_t>(S) ? loads_issued : S;
+      for (uint32_t j = loads_issued - n; j < loads_issued; ++j) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(smem_u32(&full_bar[j % S]), (j / S) & 1u))
+          if (global_timer_ns() - t0 > drain_ns) break;
+      }
+    }
+    if (warp >= 1 && warp <= C::kIssuers && lane == 0) mma_commit(smem_u32(drain_bar));
+    if (warp == 1 && lane == 0) {
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_u32(drain_bar), 0))
+        if (global_timer_ns() - t0 > drain_ns) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still read its partial
+}
+
+// Largest number of co-resident clusters of `split` CTAs for this kernel.
+template <int BN>
+int max_active_clusters(int split, size_t smem) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplit + 1] = {};
+  if (split < 1 || split > kMaxSplit) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][split] == 0) {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(split * 256, 1, 1);
+    cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = -1;
+    }
+    cache[dev][split] = n;
+  }
+  return cache[dev][split];
+}
+
+struct Plan {
+  int split = 0;
+  int clusters = 0;
+  double cost = 1e300;
+};
+
+// Launch geometry for tile width BN: shared memory, stages, and the K split
+// with the least modelled time. Returns false if BN does not fit.
+template <int BN>
+bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_out, Plan& plan) {
+  using C = SCfg<BN>;
+  args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
+  const uint32_t stage_bytes = args.a_stage_bytes + C::kBTileBytes;
+  const size_t part_bytes = static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  const size_t bar_bytes = (2 * kMaxStages + 2 * C::kNumPBuf + 3) * sizeof(uint64_t) + 32;
+  if (part_bytes + bar_bytes + 1024 >= kMaxDynSmem) return false;
+  const size_t budget = kMaxDynSmem - 1024 - part_bytes - bar_bytes;
+  auto ring_bytes = [&](int st) {
+    return std::max<size_t>(static_cast<size_t>(st) * stage_bytes,
+                            static_cast<size_t>(st - 1) * args.a_stage_bytes + kATileBytes);
+  };
+  int stages = std::min<int>(kMaxStages, static_cast<int>(budget / stage_bytes));
+  while (stages > C::kIssuers && ring_bytes(stages) > budget) --stages;
+  stages = stages / C::kIssuers * C::kIssuers;  // whole stage sets per issuer
+  if (stages < std::max(C::kIssuers, 4) || ring_bytes(stages) > budget) return false;
+  args.num_stages = stages;
+  size_t smem = 1024 + ring_bytes(stages) + part_bytes + bar_bytes;
+  smem = std::max<size_t>(smem, kMinSmemPerCta);
+  if (smem > kMaxDynSmem) return false;
+  smem_out = smem;
+
+  // Model (measured on GB300 with TMA streams of 128-byte rows): one SM
+  // streams ~45 GB/s; all SMs together ~4.8 TB/s with 128-row boxes and
+  // ~5.4 TB/s with 256-row boxes; a cluster reduction costs ~2 us per tile
+  // (mostly waiting for the slowest peer). Time = max(whole-GPU stream of B,
+  // the slowest cluster's K range per tile + its reductions).
+  const double sm_bytes_per_us = 4.5e4;
+  const double gpu_bytes_per_us = (BN == 256) ? 5.4e6 : 4.8e6;
+  const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
+  for (int split = 1; split <= kMaxSplit; ++split) {
+    if (split > args.num_kb || (BN / 8) / split < 1) break;
+    const int active = max_active_clusters<BN>(split, smem);
+    if (active <= 0) continue;
+    int clusters = std::min(active, args.num_nb);
+    if (p.num_sms_cap > 0) clusters = std::min(clusters, std::max(1, p.num_sms_cap / split));
+    if (clusters <= 0 || clusters * split > sms * 2) continue;
+    const int waves = (args.num_nb + clusters - 1) / clusters;
+    const int kbs = (args.num_kb + split - 1) / split;
+    const double per_cluster =
+        waves * (kbs * static_cast<double>(C::kBTileBytes) / sm_bytes_per_us + (split > 1 ? 2.0 : 0.0));
+    const double cost = std::max(b_bytes / gpu_bytes_per_us, per_cluster) * (1.0 + 0.01 * split);
+    if (cost < plan.cost) {
+      plan.cost = cost;
+      plan.split = split;
+      plan.clusters = clusters;
+    }
+  }
+  return plan.split > 0;
+}
+
+// Allows the kernel its shared memory on the current device (once per device);
+// the occupancy query of the planner needs it too.
+template <int BN>
+bool set_smem_attribute() {
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (attr_set.load() & (1ull << dev)) return true;
+  if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kMaxDynSmem)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  attr_set.fetch_or(1ull << dev);
+  return true;
+}
+
+template <int BN>
+int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_t smem, const Plan& plan) {
+  args.split = plan.split;
+  args.num_clusters = plan.clusters;
+  CUtensorMap ta, tb;
+  const uint32_t a_rows = args.a_box_bytes / kBK;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_a)};
+    const uint32_t box[2] = {kBK, a_rows};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box, true))
+      return DG_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_b)};
+    const uint32_t box[2] = {kBK, static_cast<uint32_t>(BN)};
+    if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
+      return DG_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = args.split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(args.split * args.num_clusters, 1, 1);
+  cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fp8_gemm_splitk_kernel<BN>, ta, tb, args) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  return DG_OK;
+}
+
+}  // namespace
+
+bool small_m_supported(int64_t M, const void* m_indices) { return m_indices == nullptr && M >= 1 && M <= kBM; }
+
+int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return DG_ERR_NO_DEVICE;
+  unsigned int* status = device_status_word();
+  if (!status) return DG_ERR_CUDA;
+
+  SmallArgs args{};
+  args.c = static_cast<__nv_bfloat16*>(p.c);
+  args.ld_c = p.ld_c;
+  args.sa = p.sa;
+  args.sb = p.sb;
+  args.status = status;
+  args.M = static_cast<int>(p.M);
+  args.N = static_cast<int>(p.N);
+  args.num_kb = static_cast<int>(p.K / kBK);
+  args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+  args.m_pad = static_cast<int>((p.M + 31) / 32 * 32);
+  const uint32_t a_rows = static_cast<uint32_t>((p.M + 7) / 8 * 8);
+  args.a_box_bytes = a_rows * kBK;
+  args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
+
+  // 256-column tiles (fewer, larger TMA boxes) when the partial tile fits.
+  if (!set_smem_attribute<256>() || !set_smem_attribute<128>()) return DG_ERR_CUDA;
+  SmallArgs a256 = args, a128 = args;
+  size_t s256 = 0, s128 = 0;
+  Plan p256, p128;
+  const bool ok256 = plan_small_m<256>(p, sms, a256, s256, p256);
+  const bool ok128 = plan_small_m<128>(p, sms, a128, s128, p128);
+  if (ok256 && (!ok128 || p256.cost <= p128.cost)) return run_small_m<256>(p, stream, a256, s256, p256);
+  if (ok128) return run_small_m<128>(p, stream, a128, s128, p128);
+  return DG_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace dg
