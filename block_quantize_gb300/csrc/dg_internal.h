@@ -32,6 +32,10 @@ struct GemmProblem {
 // Returns a dg_status value.
 int launch_gemm(const GemmProblem& p, cudaStream_t stream);
 
+// Dense GEMMs with M > 128 on CTA pairs (gemm_pair.cu); DG_ERR_UNSUPPORTED_SHAPE
+// when the problem or the launch limits do not allow a pair kernel.
+int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream);
+
 // Dense GEMMs with M <= 128 use the cluster split-K kernel (gemm_smallm.cu).
 bool small_m_supported(int64_t M, const void* m_indices);
 int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream);
@@ -49,6 +53,11 @@ cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
                        const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
                        bool swizzle128);
+
+// Same with an explicit swizzle mode.
+bool encode_tensor_map_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                               const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                               CUtensorMapSwizzle swizzle);
 
 // Device address of the current device's status word (resolved once per device
 // with cudaGetSymbolAddress); nullptr on failure.

@@ -395,9 +395,24 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA store at
         // (col0 + 32 h, mb*128 + lg*32), clipped at M and N; the two halves
         // of the slice share the box in turn. Only this warp touches it.
+        // A box that crosses column N is written element by element instead:
+        // the swizzled store clips N only to whole 16-byte chunks.
         const int row0 = mb * kBM + lg * 32;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          const int bcol = col0 + 32 * h;
+          if (bcol + 32 > args.N) {
+            if (row < args.M && bcol < args.N) {
+              __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float2 v = zero_row ? make_float2(0.f, 0.f) : f32x2_split(acc[h * 16 + j]);
+                if (bcol + 2 * j < args.N) crow[bcol + 2 * j] = __float2bfloat16_rn(v.x);
+                if (bcol + 2 * j + 1 < args.N) crow[bcol + 2 * j + 1] = __float2bfloat16_rn(v.y);
+              }
+            }
+            continue;
+          }
           if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
           __syncwarp();
           uint8_t* my_row = out_box + lane * 64;
@@ -415,8 +430,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && part_valid && row0 < args.M && col0 + 32 * h < args.N) {
-            tma_store_2d(&tmap_c, smem_u32(out_box), col0 + 32 * h, row0);
+          if (lane == 0 && part_valid && row0 < args.M) {
+            tma_store_2d(&tmap_c, smem_u32(out_box), bcol, row0);
             bulk_commit();
             stores_issued = true;
           }
@@ -665,6 +680,13 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
                        const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
                        bool swizzle128) {
+  return encode_tensor_map_swizzle(map, dtype, base, rank, dims, strides, box,
+                                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool encode_tensor_map_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                               const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                               CUtensorMapSwizzle swizzle) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], st[4];
@@ -676,9 +698,8 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
     if (i + 1 < rank) st[i] = strides[i];
   }
   const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, st, b, e,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -704,6 +725,10 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   const int sms = device_info(dev).num_sms;
   if (sms <= 0) return DG_ERR_NO_DEVICE;
   if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
+  if (!block_n_override() && p.m_indices == nullptr && p.M > kBM) {
+    const int r = launch_gemm_pair(p, stream);
+    if (r != DG_ERR_UNSUPPORTED_SHAPE) return r;
+  }
   const int bn = pick_bn(p.M, p.N, sms);
   const bool grouped = p.m_indices != nullptr;
   switch (bn) {
