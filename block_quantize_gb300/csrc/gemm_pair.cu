@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
     bool stores_issued = false;
     uint32_t it = 0;
     bool ok = true;
+    bool ready = false;  // the full barrier of slot `it` is known to be complete
     for (int t = pair; t < num_tiles && ok; t += num_pairs) {
       int pm, nb;
       pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
@@ -256,13 +257,15 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
       uint64_t acc[EC / 2];  // FP32 accumulators, two columns per register pair
 #pragma unroll
       for (int j = 0; j < EC / 2; ++j) acc[j] = 0ull;
+      float s = __ldg(sa_p) * __ldg(sb_p);
       for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
-        const float s = __ldg(sa_p + kb) * __ldg(sb_p + kb);
         const uint32_t buf = it % kNumBuf;
-        const bool w = mbar_wait(smem_u32(&tfull_bar[buf]), (it / kNumBuf) & 1u, abort_flag, status, limit);
-        if (!__all_sync(0xFFFFFFFFu, w)) {
-          ok = false;
-          break;
+        if (!ready) {
+          const bool w = mbar_wait(smem_u32(&tfull_bar[buf]), (it / kNumBuf) & 1u, abort_flag, status, limit);
+          if (!__all_sync(0xFFFFFFFFu, w)) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
         uint32_t r[EC];
@@ -272,9 +275,16 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + buf * 8u);
+        // Look ahead: test the next slot's barrier and fetch its scales now, so
+        // that their latency hides behind the multiply-adds below.
+        const uint32_t nx = it + 1;
+        const bool next_done = mbar_test(smem_u32(&tfull_bar[nx % kNumBuf]), (nx / kNumBuf) & 1u);
+        const float s_next = kb + 1 < args.num_kb ? __ldg(sa_p + kb + 1) * __ldg(sb_p + kb + 1) : 0.f;
         const uint64_t s2 = f32x2(__float_as_uint(s), __float_as_uint(s));
 #pragma unroll
         for (int j = 0; j < EC / 2; ++j) ffma2(acc[j], s2, f32x2(r[2 * j], r[2 * j + 1]));
+        ready = __all_sync(0xFFFFFFFFu, next_done);
+        s = s_next;
       }
       if (!ok) break;
 
