@@ -26,6 +26,7 @@ bounded sample of the same workload: the first 128 rows of every activation
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -83,9 +84,10 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons; the
+    summary keeps the samples taken inside the window given to stop()."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -99,7 +101,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -111,7 +113,7 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -121,25 +123,29 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-                power.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
             except ValueError:
                 continue
-            for name, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+        # A timed region shorter than the sampling period: keep the sample
+        # nearest to its middle.
+        if not inside and rows and window:
+            mid = 0.5 * (window[0] + window[1])
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        use = inside if window else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in use for n, v in zip(names, r[4]) if v.lower().startswith("active")}
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "power_w_max": max(r[3] for r in use) if use else None,
+                "samples": len(use), "samples_total": len(rows), "reasons": sorted(reasons)}
 
 
 def cpu_sample(rows_per_shape: int, reps: int = 1):
@@ -251,12 +257,14 @@ def run_ours(args):
     if clocks:
         clocks.start()
         time.sleep(0.3)
+    w0 = time.time()
     t0.record(stream)
     for s in range(args.steps):
         step(ev[s])
     t1.record(stream)
     barrier()
-    clock_info = clocks.stop() if clocks else None
+    w1 = time.time()
+    clock_info = clocks.stop((w0, w1)) if clocks else None
     ms = t0.elapsed_time(t1)
     gemm_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(shapes()))]
                for s in range(args.steps)]
@@ -362,6 +370,32 @@ def _time_each(stream, fns, iters, warmup):
     return [statistics.median(ms[i::len(fns)]) for i in range(len(fns))]
 
 
+def _time_graph(stream, fns, reps):
+    """Per-launch time of back-to-back launches replayed from one CUDA graph
+    (host launch cost excluded)."""
+    import torch
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for f in fns:
+                f()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(fns))
+
+
 def _rand_fp8(shape, dev, gen, mode):
     import torch
     import block_quantize_gb300 as bq
@@ -416,9 +450,13 @@ def run_aux(args):
                 qa, sa = _rand_fp8((m, k), dev, gen, 0)
                 c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
                 fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb) for qb, sb in bs]
-                ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+                ms_event = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+                # Launches of a few microseconds: time them back to back from a
+                # CUDA graph (rotating B copies, so every launch reads HBM).
+                ms = _time_graph(stream, fns * max(1, 24 // len(fns)), max(args.steps, 10))
                 byts = m * k + n * k + 2 * m * n + 4 * (-(-m // 128) + -(-n // 128)) * (k // 128)
-                res.append({"M": m, "N": n, "K": k, "us": ms * 1e3, "gbs": byts / (ms * 1e-3) / 1e9,
+                res.append({"M": m, "N": n, "K": k, "us": ms * 1e3, "us_single_launch": ms_event * 1e3,
+                            "gbs": byts / (ms * 1e-3) / 1e9,
                             "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
                             "tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12})
             del bs
@@ -467,13 +505,16 @@ def run_aux(args):
 def main():
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=None,
+                   help="timed steps (default 400 for this library's kernels, 20 for the CPU reference)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
                         "quantize[:R,C] | grouped  (the others print per-kernel numbers for profiling)")
     args = p.parse_args()
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 400
     if args.impl == "reference":
         return run_reference(args)
     if args.workload != "llm":
