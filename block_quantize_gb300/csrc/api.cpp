@@ -149,6 +149,7 @@ DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
   p.N = N;
   p.K = K;
   p.num_sms_cap = g_num_sms_cap.load();
+  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
   return dg::launch_gemm(p, st);
 }
 
@@ -182,6 +183,7 @@ DG_API int dg_fp8_grouped_gemm_contiguous(void* c, int64_t ld_c, const uint8_t* 
   p.N = N;
   p.K = K;
   p.num_sms_cap = g_num_sms_cap.load();
+  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
   return dg::launch_gemm(p, st);
 }
 

@@ -207,8 +207,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 2-D tile load into this CTA's shared memory whose bytes are counted on the
+// 3-D tile load into this CTA's shared memory whose bytes are counted on the
 // mbarrier at cluster address `bar_cluster`, which may be the peer CTA's.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// 2-D form of the same.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar_cluster, int32_t x, int32_t y) {
   asm volatile(
@@ -312,6 +322,34 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
                    bar)
                : "memory");
 }
+
+// Block-scaled pair MMA (kind::mxf8f6f4, one UE8M0 scale per 32 K elements of
+// each row of A and column of B, read from TMEM at sfa_tmem / sfb_tmem): the
+// tensor core multiplies each product by 2^(ea-127) 2^(eb-127) before adding.
+__device__ __forceinline__ void mma_e4m3_pair_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of the block-scaled kind::mxf8f6f4 MMA: E4M3 x E4M3,
+// both K-major, UE8M0 scale factors (bit 23), scale-factor byte 0 of each
+// TMEM word, F32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_e4m3_block_scaled(int m, int n) {
+  return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+// Store eight 32-bit columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3,
+                                         uint32_t v4, uint32_t v5, uint32_t v6, uint32_t v7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3), "r"(v4), "r"(v5), "r"(v6), "r"(v7)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

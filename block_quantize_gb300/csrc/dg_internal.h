@@ -27,6 +27,7 @@ struct GemmProblem {
   int num_groups;            // 1 for the dense GEMM
   int64_t M, N, K;
   int num_sms_cap;           // 0 = every SM
+  bool pow2_scales;          // every scale is a power of two (DG_SCALE_UE8M0)
 };
 
 // Returns a dg_status value.

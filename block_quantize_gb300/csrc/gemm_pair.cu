@@ -68,7 +68,7 @@ struct PCfg {
   static constexpr int kEpiWarps = 4 * kEpiPerQuad;
   static constexpr int kFirstEpiWarp = 1 + kIssuers;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-  static constexpr uint32_t kOutBytes = kEpiWarps * kBoxBytes;
+  static constexpr uint32_t kOutBytes = kEpiWarps * kBoxBytes * (kEpiCols / 32);
   static_assert(kEpiCols == 32 || kEpiCols == 64, "epilogue slice");
   static_assert(kThreads <= 1024, "CTA size");
 };
@@ -108,6 +108,95 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > limit_ns) break;
+  }
+}
+
+// TMA producer of both pair kernels, run by one thread per CTA. CTA r loads
+// A rows [256 pm + 128 r, +128) and B rows [128 nb + 64 r, +64) of each K
+// block into ring stage it % S; both CTAs' bytes count on the even CTA's
+// `full` barrier, which the even CTA arms for the pair. The thread shares its
+// SM sub-partition with busy warps and each TMA issue blocks it for a few
+// hundred cycles, so stage and phase are running counters. Returns the number
+// of stages it filled.
+__device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                                  const PairArgs& args, uint32_t ring0, uint64_t* full_bar,
+                                                  uint64_t* empty_bar, uint32_t rank, int pair, int num_pairs,
+                                                  volatile int* abort_flag, unsigned int* status) {
+  const int S = args.num_stages;
+  const bool leader = rank == 0;
+  const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+  const uint32_t empty0 = smem_u32(empty_bar);
+  const int num_tiles = args.num_pm * args.num_nb;
+  uint32_t stage = 0, phase = 0, issued = 0;
+  for (int t = pair; t < num_tiles; t += num_pairs) {
+    int pm, nb;
+    pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+    const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
+    const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
+    for (int kb = 0; kb < args.num_kb; ++kb) {
+      if (!mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, args.wait_limit_ns)) return issued;
+      if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
+      const uint32_t fb = leader_full + stage * 8u;
+      const uint32_t dst = ring0 + stage * kStageBytes;
+      tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
+      tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
+      ++issued;
+      if (++stage == static_cast<uint32_t>(S)) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  return issued;
+}
+
+// bf16 epilogue of one warp: its 32 rows x EC columns of acc (two FP32 per
+// 64-bit pair) -> 64-byte-swizzled 32 x 32 boxes in shared memory (16-byte
+// chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA stores, clipped at M.
+// A box that crosses column N is written element by element instead: the
+// swizzled store clips N only to whole 16-byte chunks.
+template <int EC>
+__device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], const CUtensorMap& tmap_c,
+                                                const PairArgs& args, uint8_t* out_box, int row0, int col0,
+                                                int lane, bool& stores_issued) {
+  if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last tile's stores have read the boxes
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < EC / 32; ++h) {
+    const int bcol = col0 + 32 * h;
+    if (bcol + 32 > args.N) {
+      const int row = row0 + lane;
+      if (row < args.M && bcol < args.N) {
+        __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 v = f32x2_split(acc[h * 16 + j]);
+          if (bcol + 2 * j < args.N) crow[bcol + 2 * j] = __float2bfloat16_rn(v.x);
+          if (bcol + 2 * j + 1 < args.N) crow[bcol + 2 * j + 1] = __float2bfloat16_rn(v.y);
+        }
+      }
+      continue;
+    }
+    uint8_t* box = out_box + h * kBoxBytes;
+    uint8_t* my_row = box + lane * 64;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float2 v0 = f32x2_split(acc[h * 16 + c * 4]), v1 = f32x2_split(acc[h * 16 + c * 4 + 1]);
+      const float2 v2 = f32x2_split(acc[h * 16 + c * 4 + 2]), v3 = f32x2_split(acc[h * 16 + c * 4 + 3]);
+      uint4 pk;
+      pk.x = pack_bf16(v0.x, v0.y);
+      pk.y = pack_bf16(v1.x, v1.y);
+      pk.z = pack_bf16(v2.x, v2.y);
+      pk.w = pack_bf16(v3.x, v3.y);
+      *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < args.M) {
+      tma_store_2d(&tmap_c, smem_u32(box), bcol, row0);
+      bulk_commit();
+      stores_issued = true;
+    }
   }
 }
 
@@ -168,35 +257,9 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    // Lane 0 works; the warp shares its SM sub-partition with busy epilogue
-    // warps, so the loop keeps its stage and phase in running counters.
-    if (lane == 0) {
-      const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
-      const uint32_t empty0 = smem_u32(empty_bar);
-      const uint32_t ring0 = smem_u32(ring);
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        int pm, nb;
-        pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
-        const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
-        for (int kb = 0; kb < args.num_kb; ++kb) {
-          ok = mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, limit);
-          if (!ok) break;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
-          const uint32_t fb = leader_full + stage * 8u;
-          const uint32_t dst = ring0 + stage * kStageBytes;
-          tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
-          tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
-          ++loads_issued;
-          if (++stage == static_cast<uint32_t>(S)) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-    }
+    if (lane == 0)
+      loads_issued = pair_producer(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
+                                   num_pairs, abort_flag, status);
     __syncwarp();
   } else if (warp <= kIssuers) {
     // ----------------------------------------------------------- MMA issue --
@@ -243,7 +306,7 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + part * EC;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty_bar), 0);
-    uint8_t* out_box = smem_out + ew * kBoxBytes;
+    uint8_t* out_box = smem_out + ew * kBoxBytes * (EC / 32);
     bool stores_issued = false;
     uint32_t it = 0;
     bool ok = true;
@@ -288,50 +351,8 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
       }
       if (!ok) break;
 
-      // bf16 row segment -> this warp's 64-byte-swizzled 32 x 32 box (16-byte
-      // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA store, clipped at M.
-      // A box that crosses column N is written element by element instead: the
-      // swizzled store clips N only to whole 16-byte chunks.
       const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
-      const int col0 = nb * kBN + part * EC;
-#pragma unroll
-      for (int h = 0; h < EC / 32; ++h) {
-        const int bcol = col0 + 32 * h;
-        if (bcol + 32 > args.N) {
-          const int row = row0 + lane;
-          if (row < args.M && bcol < args.N) {
-            __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 v = f32x2_split(acc[h * 16 + j]);
-              if (bcol + 2 * j < args.N) crow[bcol + 2 * j] = __float2bfloat16_rn(v.x);
-              if (bcol + 2 * j + 1 < args.N) crow[bcol + 2 * j + 1] = __float2bfloat16_rn(v.y);
-            }
-          }
-          continue;
-        }
-        if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
-        __syncwarp();
-        uint8_t* my_row = out_box + lane * 64;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float2 v0 = f32x2_split(acc[h * 16 + c * 4]), v1 = f32x2_split(acc[h * 16 + c * 4 + 1]);
-          const float2 v2 = f32x2_split(acc[h * 16 + c * 4 + 2]), v3 = f32x2_split(acc[h * 16 + c * 4 + 3]);
-          uint4 pk;
-          pk.x = pack_bf16(v0.x, v0.y);
-          pk.y = pack_bf16(v1.x, v1.y);
-          pk.z = pack_bf16(v2.x, v2.y);
-          pk.w = pack_bf16(v3.x, v3.y);
-          *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < args.M) {
-          tma_store_2d(&tmap_c, smem_u32(out_box), bcol, row0);
-          bulk_commit();
-          stores_issued = true;
-        }
-      }
+      store_tile_rows<EC>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane, stores_issued);
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
@@ -365,14 +386,341 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
   }
 }
 
-// Largest number of co-resident CTA pairs (cached per device).
-int max_active_pairs(size_t smem) {
+// ---------------------------------------------------------------------------
+// Power-of-two scales: the tensor core applies them (block-scaled MMA).
+//
+// With every scale a power of two, sa * sb * sum(a b) equals the sum of the
+// products (a 2^ea)(b 2^eb) exactly, which is what tcgen05.mma
+// kind::mxf8f6f4.block_scale computes from UE8M0 scale factors (one per 32 K
+// elements of each row of A and column of B). A 128x128 scale block gives all
+// 128 rows (columns) and all four 32-element K slices of a K block the same
+// factor, so each K block needs one exponent byte for A and one for B, written
+// into every lane and byte of a few TMEM columns. The tile's partial sums then
+// stay in TMEM across all K blocks and the epilogue reads them once per tile.
+// Without the per-K-block promotion the limits are the issuing threads: each
+// TMA issue and each MMA issue blocks its thread (the MMA until the tensor pipe
+// takes it), so
+//   * warps 0 and 3: TMA producers, alternating ring stages; a stage holds two
+//     K blocks (one 3-D box of A and one of B per CTA), counted on the even
+//     CTA's `full` barrier;
+//   * warps 1-2 of the even CTA: MMA issue, alternating stages. Per valid K
+//     block four block-scaled MMAs go into the tile's accumulator (two
+//     accumulators alternate between tiles); each stage's MMAs are committed to
+//     its `empty` barrier and each issuer commits the accumulator after its
+//     last stage of the tile. The first MMA of a tile overwrites the
+//     accumulator, so the MMAs must reach the pipe in K-block order: the
+//     issuers pass a turn counter in shared memory (deterministic results);
+//   * warps 4-7 (one per TMEM lane quadrant): write each stage's exponents
+//     (this CTA's A block, the tile's B block) into the stage's TMEM scale
+//     columns; they wait on the stage's `empty` barrier like the producers and
+//     arrive on its `full` barrier, which thus completes when both CTAs'
+//     operands and scales are in place;
+//   * warps 8-15: per tile, read the accumulator, release it, round to bf16
+//     and store.
+// A stage past an odd number of K blocks holds a zero-filled K block that gets
+// no MMA and no scale.
+// ---------------------------------------------------------------------------
+constexpr int kNatKbPerStage = 2;
+constexpr uint32_t kNatStageBytes = kNatKbPerStage * kStageBytes;  // A [2][128][128 B], B [2][64][128 B]
+constexpr uint32_t kNatAStageBytes = kNatKbPerStage * kABytes;
+constexpr int kNatMaxStages = 8;
+constexpr uint32_t kSfCols = 8;                        // 4 columns for A, 4 for B, per K block
+constexpr uint32_t kAccCols = 2 * kBN;                 // two tile accumulators
+constexpr uint32_t kIdescScaled = idesc_e4m3_block_scaled(2 * kBM, kBN);
+constexpr int kNatEpiWarps = 8;                        // 4 quadrants x 2 slices of 64 columns
+constexpr int kNatFirstEpiWarp = 8;
+constexpr int kNatThreads = 32 * (kNatFirstEpiWarp + kNatEpiWarps);
+constexpr uint32_t kNatOutBytes = kNatEpiWarps * kBoxBytes * 2;
+static_assert(kAccCols + kNatMaxStages * kNatKbPerStage * kSfCols <= 512, "TMEM");
+
+// Biased exponent of a power-of-two FP32 scale = its UE8M0 code (2^-127,
+// stored as an FP32 subnormal, has code 0), replicated into four bytes.
+__device__ __forceinline__ uint32_t ue8m0_word(float s) {
+  return 0x01010101u * ((__float_as_uint(s) >> 23) & 0xFFu);
+}
+
+__global__ void __launch_bounds__(kNatThreads, 1)
+    fp8_gemm_pair_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                const __grid_constant__ CUtensorMap tmap_b,
+                                const __grid_constant__ CUtensorMap tmap_c, const PairArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = args.num_stages;
+  uint8_t* ring = smem;
+  uint8_t* smem_out = smem + static_cast<size_t>(S) * kNatStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + kNatOutBytes);
+  uint64_t* full_bar = bars;                       // even CTA: operands and scales of both CTAs
+  uint64_t* empty_bar = bars + kNatMaxStages;      // the stage's MMAs are done
+  uint64_t* tfull_bar = bars + 2 * kNatMaxStages;  // [2] the tile's accumulator is final
+  uint64_t* tempty_bar = tfull_bar + 2;            // [2] even CTA: both epilogues read it
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* issue_turn = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  const uint64_t limit = args.wait_limit_ns;
+  unsigned int* status = args.status;
+  const int nst = (args.num_kb + kNatKbPerStage - 1) / kNatKbPerStage;  // stages per tile
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1 + 2 * 4);  // producer (with bytes) + 4 scale writers per CTA
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), nst >= 2 ? 2 : 1);  // one commit per issuer with stages in the tile
+      mbar_init(smem_u32(&tempty_bar[b]), 2 * kNatEpiWarps);
+    }
+    mbar_init(smem_u32(drain_bar), 2);
+    *abort_flag = 0;
+    *issue_turn = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_c);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = args.num_pm * args.num_nb;
+  uint32_t loads_issued = 0;
+
+  if (warp == 0 || warp == 3) {
+    // ----------------------------------------------------------- producers --
+    if (lane == 0) {
+      const uint32_t me = warp == 0 ? 0u : 1u;
+      const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+      const uint32_t empty0 = smem_u32(empty_bar), ring0 = smem_u32(ring);
+      uint32_t g = 0, stage = me, phase = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+        int pm, nb;
+        pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+        const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
+        for (int sl = 0; sl < nst; ++sl, ++g) {
+          if ((g & 1u) != me) continue;
+          ok = mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, limit);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kNatStageBytes);
+          const uint32_t fb = leader_full + stage * 8u;
+          const uint32_t dst = ring0 + stage * kNatStageBytes;
+          tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * kNatKbPerStage);
+          tma_load_3d_pair(dst + kNatAStageBytes, &tmap_b, fb, 0, brow, sl * kNatKbPerStage);
+          ++loads_issued;
+          stage += 2;
+          if (stage >= static_cast<uint32_t>(S)) {
+            stage -= S;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // ----------------------------------------------------------- MMA issue --
+    if (leader && lane == 0) {
+      const uint32_t me = static_cast<uint32_t>(warp - 1);
+      const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
+      const uint32_t ring0 = smem_u32(ring);
+      uint32_t g = 0, stage = me, sphase = 0, tl = 0;  // this issuer's stages: index parity me
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
+        const uint32_t abuf = tl & 1u;
+        const uint32_t d = tmem_base + abuf * kBN;
+        for (int sl = 0; sl < nst; ++sl, ++g) {
+          if ((g & 1u) != me) continue;
+          ok = mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit);
+          if (ok && sl == 0)
+            ok = mbar_wait(smem_u32(&tempty_bar[abuf]), ((tl >> 1) & 1u) ^ 1u, abort_flag, status, limit);
+          // Wait for the other issuer to have handed the tensor pipe stage g - 1.
+          if (ok && *issue_turn != g) {
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t i = 0; *issue_turn != g; ++i) {
+              if ((i & 63u) == 63u && (*abort_flag || global_timer_ns() - t0 > limit)) {
+                if (!*abort_flag) {
+                  *abort_flag = 1;
+                  atomicOr(status, kStatusTimeout);
+                }
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t base = ring0 + stage * kNatStageBytes;
+#pragma unroll
+          for (int j = 0; j < kNatKbPerStage; ++j) {
+            const int kb = sl * kNatKbPerStage + j;
+            if (kb < args.num_kb) {
+              const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
+              const uint64_t bdesc = sw128_kmajor_desc(base + kNatAStageBytes + j * kBHalfBytes);
+              const uint32_t sfa = tmem_base + kAccCols + (stage * kNatKbPerStage + j) * kSfCols;
+#pragma unroll
+              for (int k = 0; k < kBK / 32; ++k)
+                mma_e4m3_pair_scaled(d, adesc + 2u * k, bdesc + 2u * k, kIdescScaled, sfa, sfa + 4,
+                                     (kb > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
+          if (sl + 2 >= nst) mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
+          *issue_turn = g + 1;
+          stage += 2;
+          if (stage >= static_cast<uint32_t>(S)) {
+            stage -= S;
+            sphase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < kNatFirstEpiWarp) {
+    // ------------------------------------------------------- scale writers --
+    const uint32_t quad = warp & 3;
+    const uint32_t sf_row = tmem_base + ((quad * 32) << 16) + kAccCols;
+    const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+      int pm, nb;
+      pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+      const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
+      const float* sa_p = args.sa + static_cast<int64_t>(mb) * args.num_kb;
+      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.num_kb;
+      for (int sl = 0; sl < nst; ++sl) {
+        const int kb0 = sl * kNatKbPerStage;
+        const bool two = kb0 + 1 < args.num_kb;
+        const uint32_t ea0 = ue8m0_word(__ldg(sa_p + kb0)), eb0 = ue8m0_word(__ldg(sb_p + kb0));
+        const uint32_t ea1 = two ? ue8m0_word(__ldg(sa_p + kb0 + 1)) : ea0;
+        const uint32_t eb1 = two ? ue8m0_word(__ldg(sb_p + kb0 + 1)) : eb0;
+        const bool w = mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, status, limit);
+        if (!__all_sync(0xFFFFFFFFu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = sf_row + stage * kNatKbPerStage * kSfCols;
+        tmem_st8(col, ea0, ea0, ea0, ea0, eb0, eb0, eb0, eb0);
+        tmem_st8(col + kSfCols, ea1, ea1, ea1, ea1, eb1, eb1, eb1, eb1);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_addr(leader_full + stage * 8u);
+        if (++stage == static_cast<uint32_t>(S)) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    const int ew = warp - kNatFirstEpiWarp;
+    const int part = ew >> 2;   // columns [64 part, 64 part + 64) of the tile
+    const int quad = warp & 3;
+    const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + part * 64;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty_bar), 0);
+    uint8_t* out_box = smem_out + ew * kBoxBytes * 2;
+    bool stores_issued = false;
+    uint32_t tl = 0;
+    for (int t = pair; t < num_tiles; t += num_pairs, ++tl) {
+      int pm, nb;
+      pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+      const uint32_t abuf = tl & 1u;
+      const bool w = mbar_wait(smem_u32(&tfull_bar[abuf]), (tl >> 1) & 1u, abort_flag, status, limit);
+      if (!__all_sync(0xFFFFFFFFu, w)) break;
+      tc_fence_after();
+      uint32_t r[64];
+      tmem_ld<32>(tmem_row + abuf * kBN, &r[0]);
+      tmem_ld<32>(tmem_row + abuf * kBN + 32, &r[32]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + abuf * 8u);
+      uint64_t acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = f32x2(r[2 * j], r[2 * j + 1]);
+      const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
+      store_tile_rows<64>(acc, tmap_c, args, out_box, row0, nb * kBN + part * 64, lane, stores_issued);
+    }
+    if (lane == 0 && stores_issued) bulk_wait_all();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown --
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t drain_ns = 10000000ull;
+    if ((warp == 0 || warp == 3) && lane == 0) {
+      if (leader) {
+        // The last stages this producer filled: g = me + 2k.
+        const uint32_t me = warp == 0 ? 0u : 1u;
+        const uint32_t per = static_cast<uint32_t>(S) / 2;
+        const uint32_t n = loads_issued < per ? loads_issued : per;
+        for (uint32_t k = loads_issued - n; k < loads_issued; ++k) {
+          const uint32_t g = me + 2 * k;
+          drain_wait(smem_u32(&full_bar[g % S]), (g / S) & 1u, drain_ns);
+        }
+      } else {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+    if (leader && (warp == 1 || warp == 2) && lane == 0) mma_commit_pair(smem_u32(drain_bar));
+    if (leader && warp == 1 && lane == 0) drain_wait(smem_u32(drain_bar), 0, drain_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+// The two pair kernels: FP32 scales promoted in registers, or power-of-two
+// scales applied by the tensor core.
+using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PairArgs);
+struct PairKind {
+  PairKernel kernel;
+  int threads;
+  size_t fixed_smem;    // output staging + barriers
+  uint32_t stage_bytes;
+  int max_stages;
+  int kb_per_stage;
+};
+PairKind pair_kind(bool scaled) {
+  if (scaled)
+    return {fp8_gemm_pair_scaled_kernel, kNatThreads,
+            kNatOutBytes + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, kNatStageBytes, kNatMaxStages,
+            kNatKbPerStage};
+  return {fp8_gemm_pair_kernel<kEpiCols>, PCfg<kEpiCols>::kThreads,
+          PCfg<kEpiCols>::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes,
+          kMaxStages, 1};
+}
+
+// Largest number of co-resident CTA pairs of a kernel (cached per device).
+int max_active_pairs(bool scaled, size_t smem) {
   static std::mutex mu;
-  static int cache[64] = {};
+  static int cache[64][2] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev] == 0) {
+  int& c = cache[dev][scaled ? 1 : 0];
+  if (c == 0) {
+    const PairKind k = pair_kind(scaled);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -380,39 +728,41 @@ int max_active_pairs(size_t smem) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * 512, 1, 1);
-    cfg.blockDim = dim3(PCfg<kEpiCols>::kThreads, 1, 1);
+    cfg.blockDim = dim3(k.threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_pair_kernel<kEpiCols>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, k.kernel, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = -1;
     }
-    cache[dev] = n;
+    c = n;
   }
-  return cache[dev];
+  return c;
 }
 
-bool set_pair_smem_attribute() {
-  static std::atomic<uint64_t> done{0};
+bool set_pair_smem_attribute(bool scaled) {
+  static std::atomic<uint64_t> done[2] = {{0}, {0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (done.load() & (1ull << dev)) return true;
-  if (cudaFuncSetAttribute(fp8_gemm_pair_kernel<kEpiCols>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  std::atomic<uint64_t>& d = done[scaled ? 1 : 0];
+  if (d.load() & (1ull << dev)) return true;
+  if (cudaFuncSetAttribute(pair_kind(scaled).kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kMaxDynSmem)) != cudaSuccess)
     return false;
-  done.fetch_or(1ull << dev);
+  d.fetch_or(1ull << dev);
   return true;
 }
 
 }  // namespace
 
 int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
-  using Cf = PCfg<kEpiCols>;
   if (p.m_indices != nullptr || p.M <= kBM) return DG_ERR_UNSUPPORTED_SHAPE;
   unsigned int* status = device_status_word();
   if (!status) return DG_ERR_CUDA;
+  const bool scaled = p.pow2_scales;
+  const PairKind kind = pair_kind(scaled);
   PairArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
@@ -427,35 +777,43 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   args.num_nb = static_cast<int>((p.N + kBN - 1) / kBN);
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
-  const size_t bar_bytes = (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16;
-  const size_t budget = kMaxDynSmem - 1024 - Cf::kOutBytes - bar_bytes;
-  int stages = std::min<int>(kMaxStages, static_cast<int>(budget / kStageBytes));
-  stages = stages / kIssuers * kIssuers;  // issuer i owns the stages of index parity i
-  if (stages < 2 * kIssuers) return DG_ERR_UNSUPPORTED_SHAPE;
+  const size_t budget = kMaxDynSmem - 1024 - kind.fixed_smem;
+  int stages = std::min<int>(kind.max_stages, static_cast<int>(budget / kind.stage_bytes));
+  stages = stages / 2 * 2;  // issuer (and producer) i owns the stages of index parity i
+  if (stages < 4) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_stages = stages;
-  const size_t smem = 1024 + static_cast<size_t>(stages) * kStageBytes + Cf::kOutBytes + bar_bytes;
-  if (!set_pair_smem_attribute()) return DG_ERR_CUDA;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * kind.stage_bytes + kind.fixed_smem;
+  if (!set_pair_smem_attribute(scaled)) return DG_ERR_CUDA;
 
   const int64_t tiles = static_cast<int64_t>(args.num_pm) * args.num_nb;
-  int pairs = max_active_pairs(smem);
+  int pairs = max_active_pairs(scaled, smem);
   if (pairs <= 0) return DG_ERR_UNSUPPORTED_SHAPE;
   if (p.num_sms_cap > 0) pairs = std::min(pairs, p.num_sms_cap / 2);
   pairs = static_cast<int>(std::min<int64_t>(pairs, tiles));
   if (pairs < 1) return DG_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap ta, tb, tc;
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_a)};
-    const uint32_t box[2] = {kBK, kBM};
-    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box, true))
+  if (kind.kb_per_stage == 1) {
+    const uint64_t adims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
+    const uint64_t astr[1] = {static_cast<uint64_t>(p.ld_a)};
+    const uint32_t abox[2] = {kBK, kBM};
+    const uint64_t bdims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+    const uint64_t bstr[1] = {static_cast<uint64_t>(p.ld_b)};
+    const uint32_t bbox[2] = {kBK, kBN / 2};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, adims, astr, abox, true) ||
+        !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, bdims, bstr, bbox, true))
       return DG_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_b)};
-    const uint32_t box[2] = {kBK, kBN / 2};
-    if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
+  } else {
+    // [K/128][rows][128 bytes]: one box carries kb_per_stage K blocks.
+    const uint32_t kbs = static_cast<uint32_t>(kind.kb_per_stage);
+    const uint64_t adims[3] = {kBK, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K / kBK)};
+    const uint64_t astr[2] = {static_cast<uint64_t>(p.ld_a), kBK};
+    const uint32_t abox[3] = {kBK, kBM, kbs};
+    const uint64_t bdims[3] = {kBK, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K / kBK)};
+    const uint64_t bstr[2] = {static_cast<uint64_t>(p.ld_b), kBK};
+    const uint32_t bbox[3] = {kBK, kBN / 2, kbs};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 3, adims, astr, abox, true) ||
+        !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true))
       return DG_ERR_CUDA;
   }
   {
@@ -475,12 +833,12 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(Cf::kThreads, 1, 1);
+  cfg.blockDim = dim3(kind.threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fp8_gemm_pair_kernel<kEpiCols>, ta, tb, tc, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, kind.kernel, ta, tb, tc, args) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }

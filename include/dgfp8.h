@@ -100,7 +100,10 @@ DG_API int dg_quantize_fp8_block(const float *x, int64_t rows, int64_t cols, int
  *   a   [M][ld_a] E4M3 codes, K contiguous;  sa [ceil(M/128)][K/128] FP32
  *   b   [N][ld_b] E4M3 codes, K contiguous;  sb [ceil(N/128)][K/128] FP32
  *   scale_mode  DG_SCALE_UE8M0 promises that every scale is a power of two
- *               (it is not checked); DG_SCALE_FP32 accepts any finite scale.
+ *               >= 2^-127 (it is not checked): for M > 128 the tensor core then
+ *               applies each scale's exponent itself (block-scaled MMA), so a
+ *               scale that is not a power of two acts as its power-of-two
+ *               floor. DG_SCALE_FP32 accepts any finite scale.
  * Needs K % 128 == 0, ld_a >= K, ld_b >= K, ld_c >= N; a, b and c 16-byte
  * aligned, ld_a and ld_b multiples of 16, ld_c a multiple of 8; sa, sb 4-byte
  * aligned. M == 0 or N == 0 is a no-op; K == 0 writes zeros. */

@@ -59,6 +59,19 @@ def test_edge_shapes(oracle_mod, m, n, k):
     _check(oracle_mod, qa, sa, qb, sb, what=f"{m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (129, 136, 384), (200, 1000, 640), (256, 256, 128), (513, 257, 256), (300, 130, 1152),
+    (1024, 2112, 2048),
+])
+def test_edge_shapes_pow2_scales(oracle_mod, m, n, k):
+    """Power-of-two (UE8M0) scales: for M > 128 the tensor core applies them
+    (block-scaled MMA) instead of the FP32 promotion; ragged M and N, odd
+    numbers of K blocks."""
+    qa, sa, qb, sb = _operands(oracle_mod, m, n, k, seed=m * 5 + n + k, mode=1, dist="lognormal")
+    assert np.all(np.frexp(sa)[0] == 0.5) and np.all(np.frexp(sb)[0] == 0.5)
+    _check(oracle_mod, qa, sa, qb, sb, mode=1, what=f"{m}x{n}x{k} pow2")
+
+
 def test_output_padding_untouched(oracle_mod):
     qa, sa, qb, sb = _operands(oracle_mod, 130, 130, 256, seed=7)
     c, cbuf = _run(qa, sa, qb, sb, ldc_pad=30)
@@ -139,6 +152,25 @@ def test_num_sms_cap_is_bit_identical(oracle_mod):
         capped, _ = _run(qa, sa, qb, sb)
     finally:
         bq.dg_set_num_sms(0)
+    assert torch.equal(full.view(torch.int16), capped.view(torch.int16))
+
+
+@pytest.mark.parametrize("cap", [2, 5])
+@pytest.mark.parametrize("mnk", [(1024, 2048, 1024), (640, 1000, 384), (200, 3000, 640)])
+def test_many_tiles_per_pair_pow2_scales(oracle_mod, cap, mnk):
+    """Power-of-two scales on one or two CTA pairs: every accumulator, scale
+    slot and stage barrier goes through many phases."""
+    m, n, k = mnk
+    qa, sa, qb, sb = _operands(oracle_mod, m, n, k, seed=40 + cap, mode=1, dist="lognormal")
+    full, _ = _run(qa, sa, qb, sb, mode=1)
+    try:
+        bq.dg_set_num_sms(cap)
+        capped, _ = _run(qa, sa, qb, sb, mode=1)
+    finally:
+        bq.dg_set_num_sms(0)
+    rows = sample_rows(m, 16, seed=cap)
+    ref, mag = oracle_mod.gemm_nt(qa, sa, qb, sb, rows=rows)
+    assert_within_bound(capped[torch.as_tensor(rows, device=capped.device)], ref, mag, f"pow2 cap {cap}")
     assert torch.equal(full.view(torch.int16), capped.view(torch.int16))
 
 
