@@ -62,6 +62,14 @@ def _load():
         lib.oracle_pow2_ceil.restype = ctypes.c_float
         lib.oracle_quantize.argtypes = [f32p, i64, i64, i64, ctypes.c_int, u8p, i64, f32p]
         lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_quantize_1x128.argtypes = [f32p, i64, i64, i64, ctypes.c_int, u8p, i64, f32p]
+        lib.oracle_quantize_1x128.restype = ctypes.c_int
+        lib.oracle_gemm_nt_rows_a1x128.argtypes = [u8p, i64, f32p, u8p, i64, f32p,
+                                                   i64, i64, i64, i64p, i64, f64p, f64p]
+        lib.oracle_grouped_gemm_rows_a1x128.argtypes = [u8p, i64, f32p, u8p, f32p, i64,
+                                                        ctypes.c_void_p, i64, i64, i64,
+                                                        i64p, i64, f64p, f64p]
+        lib.oracle_grouped_gemm_rows_a1x128.restype = ctypes.c_int
         lib.oracle_gemm_nt_rows.argtypes = [u8p, i64, f32p, u8p, i64, f32p,
                                             i64, i64, i64, i64p, i64, f64p, f64p]
         lib.oracle_grouped_gemm_rows.argtypes = [u8p, i64, f32p, u8p, f32p, i64,
@@ -122,6 +130,22 @@ def quantize(x: np.ndarray, mode: int = SCALE_FP32):
     return q, s
 
 
+def quantize_1x128(x: np.ndarray, mode: int = SCALE_FP32):
+    """Row-wise 1x128 quantization of a float32 matrix (one scale per row and
+    128-column block).
+
+    Returns (q uint8 [rows, cols], scales float32 [rows, ceil(cols/128)]).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty((rows, (cols + BLOCK - 1) // BLOCK), dtype=np.float32)
+    rc = _load().oracle_quantize_1x128(_ptr(x), rows, cols, cols, int(mode), _ptr(q), cols, _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle.quantize_1x128: input holds a non-finite value")
+    return q, s
+
+
 def _rows_arg(rows, m):
     if rows is None:
         rows = np.arange(m, dtype=np.int64)
@@ -131,10 +155,11 @@ def _rows_arg(rows, m):
     return rows
 
 
-def gemm_nt(qa, sa, qb, sb, rows=None, want_e: bool = True):
+def gemm_nt(qa, sa, qb, sb, rows=None, want_e: bool = True, a_1x128: bool = False):
     """Block-scaled NT GEMM in float64: C[r, j] for i = rows[r] and all j.
 
-    qa uint8 [M, K], sa float32 [ceil(M/128), K/128], qb uint8 [N, K],
+    qa uint8 [M, K], sa float32 [ceil(M/128), K/128] (or [M, K/128] with
+    a_1x128: one A scale per row and K block), qb uint8 [N, K],
     sb float32 [ceil(N/128), K/128]. Returns (C, E) (E None if not wanted).
     """
     qa = np.ascontiguousarray(qa, dtype=np.uint8)
@@ -145,23 +170,25 @@ def gemm_nt(qa, sa, qb, sb, rows=None, want_e: bool = True):
     n, k2 = qb.shape
     if k != k2 or k % BLOCK:
         raise ValueError("K mismatch or not a multiple of 128")
-    if sa.shape != ((m + BLOCK - 1) // BLOCK, k // BLOCK) or \
-            sb.shape != ((n + BLOCK - 1) // BLOCK, k // BLOCK):
+    sa_rows = m if a_1x128 else (m + BLOCK - 1) // BLOCK
+    if sa.shape != (sa_rows, k // BLOCK) or sb.shape != ((n + BLOCK - 1) // BLOCK, k // BLOCK):
         raise ValueError("scale shape mismatch")
     rows = _rows_arg(rows, m)
     c = np.empty((rows.size, n), dtype=np.float64)
     e = np.empty((rows.size, n), dtype=np.float64) if want_e else None
-    _load().oracle_gemm_nt_rows(_ptr(qa), k, _ptr(sa), _ptr(qb), k, _ptr(sb), m, n, k,
-                                _ptr(rows), rows.size, _ptr(c),
-                                _ptr(e) if want_e else None)
+    fn = _load().oracle_gemm_nt_rows_a1x128 if a_1x128 else _load().oracle_gemm_nt_rows
+    fn(_ptr(qa), k, _ptr(sa), _ptr(qb), k, _ptr(sb), m, n, k, _ptr(rows), rows.size, _ptr(c),
+       _ptr(e) if want_e else None)
     return c, e
 
 
-def grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=None, want_e: bool = True):
+def grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=None, want_e: bool = True,
+                            a_1x128: bool = False):
     """M-grouped contiguous GEMM in float64 (rows with index -1 are zero).
 
-    qa uint8 [M_tot, K], sa float32 [M_tot/128, K/128], qb uint8 [G, N, K],
-    sb float32 [G, ceil(N/128), K/128], m_indices int32 [M_tot].
+    qa uint8 [M_tot, K], sa float32 [M_tot/128, K/128] (or [M_tot, K/128] with
+    a_1x128), qb uint8 [G, N, K], sb float32 [G, ceil(N/128), K/128],
+    m_indices int32 [M_tot].
     """
     qa = np.ascontiguousarray(qa, dtype=np.uint8)
     qb = np.ascontiguousarray(qb, dtype=np.uint8)
@@ -174,12 +201,14 @@ def grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=None, want_e: bool =
         raise ValueError("shape mismatch")
     if sb.shape != (g, (n + BLOCK - 1) // BLOCK, k // BLOCK):
         raise ValueError("sb shape mismatch")
+    if sa.shape != ((m_tot if a_1x128 else m_tot // BLOCK), k // BLOCK):
+        raise ValueError("sa shape mismatch")
     rows = _rows_arg(rows, m_tot)
     c = np.empty((rows.size, n), dtype=np.float64)
     e = np.empty((rows.size, n), dtype=np.float64) if want_e else None
-    rc = _load().oracle_grouped_gemm_rows(_ptr(qa), k, _ptr(sa), _ptr(qb), _ptr(sb), g,
-                                          _ptr(mi), m_tot, n, k, _ptr(rows), rows.size,
-                                          _ptr(c), _ptr(e) if want_e else None)
+    fn = _load().oracle_grouped_gemm_rows_a1x128 if a_1x128 else _load().oracle_grouped_gemm_rows
+    rc = fn(_ptr(qa), k, _ptr(sa), _ptr(qb), _ptr(sb), g, _ptr(mi), m_tot, n, k, _ptr(rows), rows.size,
+            _ptr(c), _ptr(e) if want_e else None)
     if rc != 0:
         raise ValueError("m_indices holds an expert id >= G")
     return c, e

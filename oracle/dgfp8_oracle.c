@@ -19,7 +19,7 @@
  *                      two), §2.3/§3.2 (M-grouped GEMM for MoE experts), §4.1
  *                      (fp8_gemm_nt(c, a, b, a_sf, b_sf) argument order).
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - E4M3 is the OCP "fn" layout: s.eeee.mmm, bias 7, no infinities, codes
  *     0x7F/0xFF are NaN; the pages fix only "E4M3" and "max 448".
  *   - "divide each element by scale" is IEEE binary32 division x / s rounded to
@@ -196,6 +196,47 @@ int oracle_quantize(const float *x, int64_t rows, int64_t cols, int64_t ld_x,
 }
 
 /* ------------------------------------------------------------------------- */
+/* Row-wise 1x128 quantizer: the same steps with blocks of one row and 128    */
+/* columns ([FP8-walkthrough] §2.3: the block granularity is a trade-off;     */
+/* [DeepGEMM-lib] §3.1: per-token activation scales beside 128x128 weight    */
+/* scales).                                                                  */
+/*   scales: float [rows][ceil(cols/128)] row-major. mode as above.           */
+/* Returns 0 on success, -1 if an input is not finite.                        */
+/* ------------------------------------------------------------------------- */
+int oracle_quantize_1x128(const float *x, int64_t rows, int64_t cols, int64_t ld_x,
+                          int mode, uint8_t *q, int64_t ld_q, float *scales)
+{
+    table_init();
+    const int64_t nbc = (cols + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *xrow = x + r * ld_x;
+        for (int64_t bj = 0; bj < nbc; ++bj) {
+            const int64_t c0 = bj * ORACLE_BLOCK;
+            const int64_t c1 = (c0 + ORACLE_BLOCK < cols) ? c0 + ORACLE_BLOCK : cols;
+            float amax = 0.0f;
+            for (int64_t c = c0; c < c1; ++c) {
+                const float ax = fabsf(xrow[c]);
+                if (!isfinite(ax))
+                    bad = 1;
+                if (ax > amax)
+                    amax = ax;
+            }
+            float s = amax / 448.0f;
+            if (s == 0.0f)
+                s = 1.0f;
+            if (mode == 1)
+                s = oracle_pow2_ceil(s);
+            scales[r * nbc + bj] = s;
+            for (int64_t c = c0; c < c1; ++c)
+                q[r * ld_q + c] = oracle_e4m3_encode(xrow[c] / s);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Block-scaled NT GEMM in double ([FP8-walkthrough] §2.2, §4.3;             */
 /* [DeepGEMM-lib] §3.1 NT layout, §4.1).                                      */
 /*   A codes qa [M][ld_a] (K contiguous), scales sa [ceil(M/128)][K/128];     */
@@ -250,6 +291,24 @@ void oracle_gemm_nt_rows(const uint8_t *qa, int64_t ld_a, const float *sa,
     }
 }
 
+/* Same with one A scale per row and K block: sa [M][K/128]. */
+void oracle_gemm_nt_rows_a1x128(const uint8_t *qa, int64_t ld_a, const float *sa,
+                                const uint8_t *qb, int64_t ld_b, const float *sb,
+                                int64_t M, int64_t N, int64_t K,
+                                const int64_t *rows, int64_t nrows,
+                                double *C, double *E)
+{
+    table_init();
+    (void)M;
+    const int64_t nkb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows[r];
+        gemm_row(qa + i * ld_a, sa + i * nkb, qb, ld_b, sb, N, K,
+                 C + r * N, E ? E + r * N : NULL);
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* M-grouped contiguous GEMM ([DeepGEMM-lib] §2.3, §3.2, §3.3).               */
 /*   A [M_tot][ld_a] with scales sa [M_tot/128][K/128]; B [G][N][K] packed    */
@@ -258,6 +317,11 @@ void oracle_gemm_nt_rows(const uint8_t *qa, int64_t ld_a, const float *sa,
 /*   Computes the requested rows like oracle_gemm_nt_rows, with B and sb of   */
 /*   expert m_indices[i]. Returns -1 if an index is >= G.                     */
 /* ------------------------------------------------------------------------- */
+static int grouped_rows(const uint8_t *qa, int64_t ld_a, const float *sa, int64_t sa_rows_per_scale,
+                        const uint8_t *qb, const float *sb, int64_t G,
+                        const int32_t *m_indices, int64_t N, int64_t K,
+                        const int64_t *rows, int64_t nrows, double *C, double *E);
+
 int oracle_grouped_gemm_rows(const uint8_t *qa, int64_t ld_a, const float *sa,
                              const uint8_t *qb, const float *sb, int64_t G,
                              const int32_t *m_indices, int64_t M_tot,
@@ -265,8 +329,29 @@ int oracle_grouped_gemm_rows(const uint8_t *qa, int64_t ld_a, const float *sa,
                              const int64_t *rows, int64_t nrows,
                              double *C, double *E)
 {
-    table_init();
     (void)M_tot;
+    return grouped_rows(qa, ld_a, sa, ORACLE_BLOCK, qb, sb, G, m_indices, N, K, rows, nrows, C, E);
+}
+
+/* Same with one A scale per row and K block: sa [M_tot][K/128]. */
+int oracle_grouped_gemm_rows_a1x128(const uint8_t *qa, int64_t ld_a, const float *sa,
+                                    const uint8_t *qb, const float *sb, int64_t G,
+                                    const int32_t *m_indices, int64_t M_tot,
+                                    int64_t N, int64_t K,
+                                    const int64_t *rows, int64_t nrows,
+                                    double *C, double *E)
+{
+    (void)M_tot;
+    return grouped_rows(qa, ld_a, sa, 1, qb, sb, G, m_indices, N, K, rows, nrows, C, E);
+}
+
+/* Rows of the grouped GEMM; A scale row of output row i is i / sa_rows_per_scale. */
+static int grouped_rows(const uint8_t *qa, int64_t ld_a, const float *sa, int64_t sa_rows_per_scale,
+                        const uint8_t *qb, const float *sb, int64_t G,
+                        const int32_t *m_indices, int64_t N, int64_t K,
+                        const int64_t *rows, int64_t nrows, double *C, double *E)
+{
+    table_init();
     const int64_t nkb = K / ORACLE_BLOCK;
     const int64_t nbn = (N + ORACLE_BLOCK - 1) / ORACLE_BLOCK;
     int bad = 0;
@@ -286,7 +371,7 @@ int oracle_grouped_gemm_rows(const uint8_t *qa, int64_t ld_a, const float *sa,
             }
             continue;
         }
-        gemm_row(qa + i * ld_a, sa + (i / ORACLE_BLOCK) * nkb,
+        gemm_row(qa + i * ld_a, sa + (i / sa_rows_per_scale) * nkb,
                  qb + (int64_t)g * N * K, K, sb + (int64_t)g * nbn * nkb, N, K,
                  crow, erow);
     }
