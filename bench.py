@@ -475,6 +475,39 @@ def run_aux(args):
             res.append({"rows": r, "cols": cdim, "mode": mode, "us": ms * 1e3,
                         "gbs": byts / (ms * 1e-3) / 1e9, "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm})
         out["results"] = res
+    elif kind == "quantize1x128":
+        # Row-wise (1x128) activation quantizer, FP32 and bfloat16 inputs.
+        r, cdim = (int(v) for v in (spec or "16384,7168").split(","))
+        q = torch.empty((r, cdim), dtype=torch.uint8, device=dev)
+        s_ = torch.empty((r, -(-cdim // 128)), dtype=torch.float32, device=dev)
+        res = []
+        for dt, esize in ((torch.float32, 4), (torch.bfloat16, 2)):
+            copies = max(1, -(-3 * L2_BYTES // (r * cdim * (esize + 1))))
+            xs = [torch.randn((r, cdim), generator=gen, device=dev).to(dt) for _ in range(copies)]
+            for mode in (0, 1):
+                fns = [lambda x=x: bq.dg_quantize_fp8_1x128(x, mode, q, s_) for x in xs]
+                ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+                byts = r * cdim * (esize + 1) + s_.numel() * 4
+                res.append({"rows": r, "cols": cdim, "input": str(dt).replace("torch.", ""), "mode": mode,
+                            "us": ms * 1e3, "gbs": byts / (ms * 1e-3) / 1e9,
+                            "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm})
+            del xs
+        out["results"] = res
+    elif kind == "gemm1x128":
+        # Dense GEMM with row-wise activation scales (sa [M][K/128]).
+        m, n, k = (int(v) for v in (spec or "4096,7168,2048").split(","))
+        qa, _ = _rand_fp8((m, k), dev, gen, 0)
+        x = torch.randn((m, k), generator=gen, device=dev)
+        qa, sa = bq.dg_quantize_fp8_1x128(x)
+        del x
+        copies = max(1, -(-3 * L2_BYTES // (n * k)))
+        bs = [_rand_fp8((n, k), dev, gen, 0) for _ in range(copies)]
+        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt_1x128(c, qa, qb, sa, sb) for qb, sb in bs]
+        ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        out["results"] = [{"M": m, "N": n, "K": k, "us": ms * 1e3, "tflops": tf,
+                           "frac_fp8_burst": tf / fp8_peak}]
     elif kind == "grouped":
         mo = synthetic.MOE
         sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
@@ -511,7 +544,8 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
-                        "quantize[:R,C] | grouped  (the others print per-kernel numbers for profiling)")
+                        "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K]  "
+                        "(the others print per-kernel numbers for profiling)")
     args = p.parse_args()
     if args.steps is None:
         args.steps = 20 if args.impl == "reference" else 400

@@ -25,7 +25,8 @@ import threading
 import torch
 
 __all__ = [
-    "DG_OK", "DG_SCALE_FP32", "DG_SCALE_UE8M0", "DgError", "lib", "library_path",
+    "DG_OK", "DG_SCALE_FP32", "DG_SCALE_UE8M0", "DG_INPUT_FP32", "DG_INPUT_BF16", "DgError", "lib",
+    "library_path",
     "dg_get_abi_version", "dg_status_string", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_set_num_sms", "dg_get_num_sms", "dg_quantize_fp8_block", "dg_fp8_gemm_nt",
     "dg_fp8_grouped_gemm_contiguous", "dg_get_device_status", "dg_selftest_wait_timeout",
@@ -45,6 +46,8 @@ DG_ERR_NO_DEVICE = 5
 DG_ERR_TIMEOUT = 6
 DG_SCALE_FP32 = 0
 DG_SCALE_UE8M0 = 1
+DG_INPUT_FP32 = 0
+DG_INPUT_BF16 = 1
 BLOCK = 128
 
 _lock = threading.Lock()
@@ -86,6 +89,12 @@ def lib() -> ctypes.CDLL:
         L.dg_fp8_grouped_gemm_contiguous.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, vp,
                                                      i64, i64, i64, i32, vp]
         L.dg_fp8_grouped_gemm_contiguous.restype = i32
+        L.dg_quantize_fp8_1x128.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, i32, vp]
+        L.dg_quantize_fp8_1x128.restype = i32
+        L.dg_fp8_gemm_nt_1x128.argtypes = L.dg_fp8_gemm_nt.argtypes
+        L.dg_fp8_gemm_nt_1x128.restype = i32
+        L.dg_fp8_grouped_gemm_contiguous_1x128.argtypes = L.dg_fp8_grouped_gemm_contiguous.argtypes
+        L.dg_fp8_grouped_gemm_contiguous_1x128.restype = i32
         L.dg_get_device_status.argtypes = [vp]
         L.dg_get_device_status.restype = i32
         L.dg_selftest_wait_timeout.argtypes = [i64, vp]
@@ -175,9 +184,46 @@ def dg_quantize_fp8_block(x: torch.Tensor, scale_mode: int = DG_SCALE_FP32,
     return q, scales
 
 
+def dg_quantize_fp8_1x128(x: torch.Tensor, scale_mode: int = DG_SCALE_FP32,
+                          q: torch.Tensor | None = None, scales: torch.Tensor | None = None):
+    """Row-wise quantization (one scale per row and 128 columns) of a float32
+    or bfloat16 CUDA matrix; returns (q uint8 [rows, cols], scales float32
+    [rows, ceil(cols/128)])."""
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
+    _cuda(x, x.dtype, "x")
+    rows, cols = x.shape
+    ld_x = _ld(x, "x", 8)
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, (cols + BLOCK - 1) // BLOCK), dtype=torch.float32, device=x.device)
+    qb = _u8(q)
+    _cuda(qb, torch.uint8, "q")
+    _cuda(scales, torch.float32, "scales")
+    if tuple(scales.shape) != (rows, (cols + BLOCK - 1) // BLOCK) or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous [rows, ceil(cols/128)] tensor")
+    dtype = DG_INPUT_BF16 if x.dtype == torch.bfloat16 else DG_INPUT_FP32
+    st = lib().dg_quantize_fp8_1x128(ctypes.c_void_p(x.data_ptr()), dtype, rows, cols, ld_x,
+                                     ctypes.c_void_p(qb.data_ptr()), _ld(qb, "q", 4),
+                                     ctypes.c_void_p(scales.data_ptr()), int(scale_mode), _stream(x))
+    _check(st, "dg_quantize_fp8_1x128")
+    return q, scales
+
+
 def dg_fp8_gemm_nt(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor,
                    sb: torch.Tensor, scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
     """c[M, N] (bf16) = block-scaled A[M, K] . B[N, K]^T; returns c."""
+    return _gemm_nt(c, a, b, sa, sb, scale_mode, False)
+
+
+def dg_fp8_gemm_nt_1x128(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor,
+                         sb: torch.Tensor, scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
+    """As dg_fp8_gemm_nt with one A scale per row and K block (sa [M, K/128])."""
+    return _gemm_nt(c, a, b, sa, sb, scale_mode, True)
+
+
+def _gemm_nt(c, a, b, sa, sb, scale_mode, a_1x128):
     a, b = _u8(a), _u8(b)
     _cuda(c, torch.bfloat16, "c")
     _cuda(a, torch.uint8, "a")
@@ -189,16 +235,18 @@ def dg_fp8_gemm_nt(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.
     if b.shape[1] != k or tuple(c.shape) != (m, n):
         raise ValueError("shape mismatch between c, a and b")
     kb = k // BLOCK
-    if tuple(sa.shape) != ((m + BLOCK - 1) // BLOCK, kb) or tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
+    sa_rows = m if a_1x128 else (m + BLOCK - 1) // BLOCK
+    if tuple(sa.shape) != (sa_rows, kb) or tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
         raise ValueError("scale shape mismatch")
     if not (sa.is_contiguous() and sb.is_contiguous()):
         raise ValueError("scales must be contiguous")
-    st = lib().dg_fp8_gemm_nt(ctypes.c_void_p(c.data_ptr()), _ld(c, "c", 8),
-                              ctypes.c_void_p(a.data_ptr()), _ld(a, "a"),
-                              ctypes.c_void_p(sa.data_ptr()),
-                              ctypes.c_void_p(b.data_ptr()), _ld(b, "b"),
-                              ctypes.c_void_p(sb.data_ptr()), m, n, k, int(scale_mode), _stream(c))
-    _check(st, "dg_fp8_gemm_nt")
+    fn = lib().dg_fp8_gemm_nt_1x128 if a_1x128 else lib().dg_fp8_gemm_nt
+    st = fn(ctypes.c_void_p(c.data_ptr()), _ld(c, "c", 8),
+            ctypes.c_void_p(a.data_ptr()), _ld(a, "a"),
+            ctypes.c_void_p(sa.data_ptr()),
+            ctypes.c_void_p(b.data_ptr()), _ld(b, "b"),
+            ctypes.c_void_p(sb.data_ptr()), m, n, k, int(scale_mode), _stream(c))
+    _check(st, "dg_fp8_gemm_nt_1x128" if a_1x128 else "dg_fp8_gemm_nt")
     return c
 
 
@@ -206,6 +254,17 @@ def dg_fp8_grouped_gemm_contiguous(c: torch.Tensor, a: torch.Tensor, b: torch.Te
                                    sa: torch.Tensor, sb: torch.Tensor, m_indices: torch.Tensor,
                                    scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
     """c[M_tot, N] = A[M_tot, K] . B[g(i)]^T per row i, zero for padding rows."""
+    return _grouped(c, a, b, sa, sb, m_indices, scale_mode, False)
+
+
+def dg_fp8_grouped_gemm_contiguous_1x128(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor,
+                                         sa: torch.Tensor, sb: torch.Tensor, m_indices: torch.Tensor,
+                                         scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
+    """As dg_fp8_grouped_gemm_contiguous with sa [M_tot, K/128] (one A scale per row and K block)."""
+    return _grouped(c, a, b, sa, sb, m_indices, scale_mode, True)
+
+
+def _grouped(c, a, b, sa, sb, m_indices, scale_mode, a_1x128):
     a, b = _u8(a), _u8(b)
     _cuda(c, torch.bfloat16, "c")
     _cuda(a, torch.uint8, "a")
@@ -218,17 +277,18 @@ def dg_fp8_grouped_gemm_contiguous(c: torch.Tensor, a: torch.Tensor, b: torch.Te
     if k2 != k or tuple(c.shape) != (m_tot, n) or tuple(m_indices.shape) != (m_tot,):
         raise ValueError("shape mismatch")
     kb = k // BLOCK
-    if tuple(sa.shape) != ((m_tot + BLOCK - 1) // BLOCK, kb) or \
-            tuple(sb.shape) != (g, (n + BLOCK - 1) // BLOCK, kb):
+    sa_rows = m_tot if a_1x128 else (m_tot + BLOCK - 1) // BLOCK
+    if tuple(sa.shape) != (sa_rows, kb) or tuple(sb.shape) != (g, (n + BLOCK - 1) // BLOCK, kb):
         raise ValueError("scale shape mismatch")
     if not (b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous() and m_indices.is_contiguous()):
         raise ValueError("b, sa, sb and m_indices must be contiguous")
-    st = lib().dg_fp8_grouped_gemm_contiguous(
+    fn = lib().dg_fp8_grouped_gemm_contiguous_1x128 if a_1x128 else lib().dg_fp8_grouped_gemm_contiguous
+    st = fn(
         ctypes.c_void_p(c.data_ptr()), _ld(c, "c", 8), ctypes.c_void_p(a.data_ptr()), _ld(a, "a"),
         ctypes.c_void_p(sa.data_ptr()), ctypes.c_void_p(b.data_ptr()),
         ctypes.c_void_p(sb.data_ptr()), g, ctypes.c_void_p(m_indices.data_ptr()),
         m_tot, n, k, int(scale_mode), _stream(c))
-    _check(st, "dg_fp8_grouped_gemm_contiguous")
+    _check(st, "dg_fp8_grouped_gemm_contiguous_1x128" if a_1x128 else "dg_fp8_grouped_gemm_contiguous")
     return c
 
 

@@ -124,9 +124,27 @@ DG_API int dg_quantize_fp8_block(const float* x, int64_t rows, int64_t cols, int
   return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
-DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
-                          const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
-                          int64_t K, int scale_mode, void* stream) {
+DG_API int dg_quantize_fp8_1x128(const void* x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x,
+                                 uint8_t* q, int64_t ld_q, float* scales, int scale_mode, void* stream) {
+  if (rows < 0 || cols < 0) return DG_ERR_INVALID_ARG;
+  if (scale_mode != DG_SCALE_FP32 && scale_mode != DG_SCALE_UE8M0) return DG_ERR_INVALID_ARG;
+  if (x_dtype != DG_INPUT_FP32 && x_dtype != DG_INPUT_BF16) return DG_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return DG_OK;  // nothing to do; pointers may be NULL
+  if (!x || !q || !scales) return DG_ERR_INVALID_ARG;
+  if (ld_x < cols || ld_q < cols) return DG_ERR_INVALID_ARG;
+  if (!aligned(x, x_dtype == DG_INPUT_BF16 ? 2 : 4) || !aligned(scales, 4)) return DG_ERR_MISALIGNED;
+  if (rows * ((cols + 127) / 128) >= (int64_t(1) << 40)) return DG_ERR_UNSUPPORTED_SHAPE;
+  const int dev_st = check_device();
+  if (dev_st != DG_OK) return dev_st;
+  const cudaError_t e = dg::launch_quantize_1x128(x, x_dtype == DG_INPUT_BF16, rows, cols, ld_x, q, ld_q,
+                                                  scales, scale_mode == DG_SCALE_UE8M0,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                      const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
+                      int scale_mode, void* stream, bool a_1x128) {
   const int v = validate_gemm_common(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode);
   if (v == kEmpty) return DG_OK;
   if (v != DG_OK) return v;
@@ -150,13 +168,25 @@ DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
   p.K = K;
   p.num_sms_cap = g_num_sms_cap.load();
   p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+  p.sa_per_row = a_1x128;
   return dg::launch_gemm(p, st);
 }
 
-DG_API int dg_fp8_grouped_gemm_contiguous(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
-                                          const float* sa, const uint8_t* b, const float* sb,
-                                          int num_groups, const int32_t* m_indices, int64_t M_tot,
-                                          int64_t N, int64_t K, int scale_mode, void* stream) {
+DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                          const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
+                          int64_t K, int scale_mode, void* stream) {
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, false);
+}
+
+DG_API int dg_fp8_gemm_nt_1x128(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                                const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
+                                int64_t K, int scale_mode, void* stream) {
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, true);
+}
+
+static int gemm_grouped(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                        const uint8_t* b, const float* sb, int num_groups, const int32_t* m_indices,
+                        int64_t M_tot, int64_t N, int64_t K, int scale_mode, void* stream, bool a_1x128) {
   const int v = validate_gemm_common(c, ld_c, a, ld_a, sa, b, K, sb, M_tot, N, K, scale_mode);
   if (v == kEmpty) return (num_groups < 1 || M_tot % 128 != 0) ? DG_ERR_INVALID_ARG : DG_OK;
   if (v != DG_OK) return v;
@@ -184,7 +214,24 @@ DG_API int dg_fp8_grouped_gemm_contiguous(void* c, int64_t ld_c, const uint8_t* 
   p.K = K;
   p.num_sms_cap = g_num_sms_cap.load();
   p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+  p.sa_per_row = a_1x128;
   return dg::launch_gemm(p, st);
+}
+
+DG_API int dg_fp8_grouped_gemm_contiguous(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
+                                          const float* sa, const uint8_t* b, const float* sb,
+                                          int num_groups, const int32_t* m_indices, int64_t M_tot,
+                                          int64_t N, int64_t K, int scale_mode, void* stream) {
+  return gemm_grouped(c, ld_c, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
+                      false);
+}
+
+DG_API int dg_fp8_grouped_gemm_contiguous_1x128(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
+                                                const float* sa, const uint8_t* b, const float* sb,
+                                                int num_groups, const int32_t* m_indices, int64_t M_tot,
+                                                int64_t N, int64_t K, int scale_mode, void* stream) {
+  return gemm_grouped(c, ld_c, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
+                      true);
 }
 
 DG_API int dg_get_device_status(void* stream) {

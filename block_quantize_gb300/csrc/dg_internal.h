@@ -13,6 +13,11 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t 
                             uint8_t* q, int64_t ld_q, float* scales, bool pow2_scales,
                             cudaStream_t stream);
 
+// Row-wise 1x128 quantizer launch (sizes already validated, rows, cols > 0).
+cudaError_t launch_quantize_1x128(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t ld_x,
+                                  uint8_t* q, int64_t ld_q, float* scales, bool pow2_scales,
+                                  cudaStream_t stream);
+
 // One dense or M-grouped GEMM problem (sizes already validated).
 struct GemmProblem {
   void* c;
@@ -28,6 +33,7 @@ struct GemmProblem {
   int64_t M, N, K;
   int num_sms_cap;           // 0 = every SM
   bool pow2_scales;          // every scale is a power of two (DG_SCALE_UE8M0)
+  bool sa_per_row;           // sa is [M][K/128] (one A scale per row and K block)
 };
 
 // Returns a dg_status value.

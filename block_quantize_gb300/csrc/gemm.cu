@@ -61,6 +61,7 @@ constexpr uint32_t kWarpOutBytes = 32 * 32 * 2;  // one warp's 32 x 32 bf16 outp
 
 struct GemmArgs {
   __nv_bfloat16* c;
+  int sa_per_row;  // sa is [M][K/128] instead of [ceil(M/128)][K/128]
   int64_t ld_c;
   const float* sa;
   const float* sb;
@@ -302,7 +303,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int col0 = nb * BN + part * kCols;
       const bool part_valid = col0 < args.N;
       const int sb_block = min(col0 / kBK, args.nbs - 1);
-      const float* sa_row = args.sa + static_cast<int64_t>(mb) * args.num_kb;
+      // This thread's row's scales (rows past M read the last row's).
+      const float* sa_row =
+          args.sa + static_cast<int64_t>(args.sa_per_row ? min(mb * kBM + row_in_tile, args.M - 1) : mb) * args.num_kb;
       const float* sb_row =
           args.sb + (static_cast<int64_t>(g) * args.nbs + sb_block) * args.num_kb;
 
@@ -592,6 +595,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
   args.sa = p.sa;
+  args.sa_per_row = p.sa_per_row ? 1 : 0;
   args.sb = p.sb;
   args.m_indices = p.m_indices;
   args.M = static_cast<int>(p.M);

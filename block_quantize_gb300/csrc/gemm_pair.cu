@@ -77,6 +77,7 @@ constexpr int kEpiCols = 64;
 struct PairArgs {
   __nv_bfloat16* c;
   int64_t ld_c;
+  int sa_per_row;  // sa is [M][K/128] instead of [ceil(M/128)][K/128]
   const float* sa;
   const float* sb;
   unsigned int* status;
@@ -315,7 +316,9 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
       int pm, nb;
       pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
-      const float* sa_p = args.sa + static_cast<int64_t>(mb) * args.num_kb;
+      // This thread's row's scales (rows past M read the last row's).
+      const int arow = min(pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32 + lane, args.M - 1);
+      const float* sa_p = args.sa + static_cast<int64_t>(args.sa_per_row ? arow : mb) * args.num_kb;
       const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.num_kb;
       uint64_t acc[EC / 2];  // FP32 accumulators, two columns per register pair
 #pragma unroll
@@ -761,12 +764,15 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   if (p.m_indices != nullptr || p.M <= kBM) return DG_ERR_UNSUPPORTED_SHAPE;
   unsigned int* status = device_status_word();
   if (!status) return DG_ERR_CUDA;
-  const bool scaled = p.pow2_scales;
+  // The block-scaled kernel fills its scale columns uniformly, which needs one
+  // A scale per 128 rows; per-row A scales take the FP32 promotion (exact too).
+  const bool scaled = p.pow2_scales && !p.sa_per_row;
   const PairKind kind = pair_kind(scaled);
   PairArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
   args.sa = p.sa;
+  args.sa_per_row = p.sa_per_row ? 1 : 0;
   args.sb = p.sb;
   args.status = status;
   args.M = static_cast<int>(p.M);

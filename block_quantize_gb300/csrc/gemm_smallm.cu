@@ -68,6 +68,7 @@ struct SCfg {
 
 struct SmallArgs {
   __nv_bfloat16* c;
+  int sa_per_row;  // sa is [M][K/128] instead of [1][K/128]
   int64_t ld_c;
   const float* sa;
   const float* sb;
@@ -234,6 +235,8 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
     const int col_hi = ((static_cast<int>(rank) + 1) * (BN / 8) / split) * 8;
     const int groups8 = (col_hi - col_lo) / 8;
     const int work = args.M * groups8;
+    // Offset of this thread's row's scales (rows past M read the last row's).
+    const int sa_off = args.sa_per_row ? min(row, args.M - 1) * args.num_kb : 0;
     uint32_t it = 0;
     uint32_t tile_seq = 0;
     bool ok = true;
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] = 0ull;
       for (int kb = kb_lo; kb < kb_hi && ok; ++kb, ++it) {
-        const float sv = valid ? __ldg(args.sa + kb) * __ldg(sb_row + kb) : 0.f;
+        const float sv = valid ? __ldg(args.sa + sa_off + kb) * __ldg(sb_row + kb) : 0.f;
         const uint32_t buf = it % C::kNumPBuf;
         const bool w = mbar_wait(smem_u32(&tfull_bar[buf]), (it / C::kNumPBuf) & 1u, abort_flag, status, limit);
         ok = __all_sync(0xFFFFFFFFu, w);
@@ -530,6 +533,7 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
   args.sa = p.sa;
+  args.sa_per_row = p.sa_per_row ? 1 : 0;
   args.sb = p.sb;
   args.status = status;
   args.M = static_cast<int>(p.M);

@@ -33,7 +33,14 @@
 //    as zeros (TMA fill), which leaves the block max unchanged.
 //  * quantize_kernel (any alignment): one CTA per block, the block held in
 //    registers between the two passes.
+//
+// The row-wise variant (blocks of 1 x 128, per-token activation scales, pzsr.cn
+// page §3.1; FP32 or bfloat16 input) gives each warp a contiguous run of
+// (row, 128-column segment) pairs: lane l holds columns [4l, 4l + 4) of a
+// segment, four segments are loaded before any is reduced, the segment max is
+// one warp reduction, and the same encode4 arithmetic produces the codes.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -180,95 +187,249 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
   }
 }
 
-constexpr int kStreamStages = 3;
-constexpr uint32_t kBlockBytes = kBlock * kBlock * 4;
+// ------------------------------------------------------------- row-wise --
+constexpr int k1xThreads = 256;
+constexpr int k1xWarps = k1xThreads / 32;
+constexpr int k1xSegs = 4;  // segments in flight per warp
 
-template <bool kPow2>
+// Four consecutive elements at column c0 of a row, widened to FP32 (exact for
+// bfloat16); columns >= cols read as 0.
+template <bool kBf16, bool kVec>
+__device__ __forceinline__ float4 load_row4(const void* __restrict__ x, int64_t row, int64_t ld_x, int64_t c0,
+                                            int64_t cols) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (kBf16) {
+    const uint16_t* p = static_cast<const uint16_t*>(x) + row * ld_x + c0;
+    if (kVec && c0 + 3 < cols) {
+      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+      v = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+    } else {
+      if (c0 < cols) v.x = __uint_as_float(static_cast<uint32_t>(p[0]) << 16);
+      if (c0 + 1 < cols) v.y = __uint_as_float(static_cast<uint32_t>(p[1]) << 16);
+      if (c0 + 2 < cols) v.z = __uint_as_float(static_cast<uint32_t>(p[2]) << 16);
+      if (c0 + 3 < cols) v.w = __uint_as_float(static_cast<uint32_t>(p[3]) << 16);
+    }
+  } else {
+    const float* p = static_cast<const float*>(x) + row * ld_x + c0;
+    if (kVec && c0 + 3 < cols) {
+      v = __ldcs(reinterpret_cast<const float4*>(p));
+    } else {
+      if (c0 < cols) v.x = p[0];
+      if (c0 + 1 < cols) v.y = p[1];
+      if (c0 + 2 < cols) v.z = p[2];
+      if (c0 + 3 < cols) v.w = p[3];
+    }
+  }
+  return v;
+}
+
+template <bool kBf16, bool kVec, bool kPow2>
+__global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* __restrict__ q, int64_t ld_q,
+    float* __restrict__ scales, int64_t nbc, int64_t per_warp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * k1xWarps + (threadIdx.x >> 5);
+  const int64_t total = rows * nbc;
+  int64_t seg = w * per_warp;
+  const int64_t end = min(total, seg + per_warp);
+  if (seg >= end) return;
+  int64_t row = seg / nbc;
+  int64_t cb = seg - row * nbc;
+  while (seg < end) {
+    float4 v[k1xSegs];
+    int64_t rr[k1xSegs], cc[k1xSegs];
+#pragma unroll
+    for (int i = 0; i < k1xSegs; ++i) {
+      rr[i] = row;
+      cc[i] = cb * kBlock + lane * 4;
+      v[i] = (seg + i < end) ? load_row4<kBf16, kVec>(x, row, ld_x, cc[i], cols) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (++cb == nbc) {
+        cb = 0;
+        ++row;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < k1xSegs; ++i) {
+      if (seg + i >= end) break;
+      const float m = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+      // Non-negative floats order like their bit patterns.
+      const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
+      float s = amax / 448.0f;
+      if (s == 0.0f) s = 1.0f;
+      if constexpr (kPow2) s = pow2_round_up(s);
+      if (lane == 0) scales[rr[i] * nbc + (cc[i] >> 7)] = s;
+      const float r = 1.0f / s;
+      uint8_t* out = q + rr[i] * ld_q + cc[i];
+      uint32_t code;
+      if constexpr (kPow2) {
+        code = encode4<1>(v[i], s, r);
+      } else if (s >= 0x1p-126f) {
+        code = encode4<0>(v[i], s, r);
+      } else {
+        code = encode4<2>(v[i], s, r);
+      }
+      if (kVec && cc[i] + 3 < cols) {
+        __stcs(reinterpret_cast<unsigned int*>(out), code);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (cc[i] + t < cols) out[t] = static_cast<uint8_t>((code >> (8 * t)) & 0xFFu);
+      }
+    }
+    seg += k1xSegs;
+  }
+}
+
+// Stages of the streaming ring: ~190 KB of input in flight per SM.
+template <bool kBf16>
+struct StreamCfg {
+  static constexpr int kElemBytes = kBf16 ? 2 : 4;
+  static constexpr uint32_t kTileBytes = kBlock * kBlock * kElemBytes;
+  static constexpr int kStages = kBf16 ? 6 : 3;
+};
+
+// kRowwise: one scale per row of the tile (1 x 128 blocks) instead of one per
+// tile; kBf16: bfloat16 input tiles, widened to FP32 exactly.
+template <bool kPow2, bool kRowwise, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     quantize_stream_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t rows, int64_t cols,
                            uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ scales,
                            int64_t blocks_per_row, int64_t nblocks, unsigned int* status,
                            uint64_t limit_ns) {
+  using SC = StreamCfg<kBf16>;
+  constexpr int kStages = SC::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  float* stage_data = reinterpret_cast<float*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStreamStages * kBlockBytes);
-  float* warp_amax = reinterpret_cast<float*>(full + kStreamStages);
+  uint8_t* stage_data = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * SC::kTileBytes);
+  float* warp_amax = reinterpret_cast<float*>(full + kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(warp_amax + kWarps);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStreamStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   int64_t issued = 0;  // thread 0: blocks whose load was issued (in order)
-  auto issue = [&](int64_t j) {  // load this CTA's j-th block into stage j % kStreamStages
+  auto issue = [&](int64_t j) {  // load this CTA's j-th block into stage j % kStages
     const int64_t blk = blockIdx.x + j * gridDim.x;
     if (blk >= nblocks) return;
     issued = j + 1;
     const int64_t bi = blk / blocks_per_row, bj = blk - bi * blocks_per_row;
-    const int st = static_cast<int>(j % kStreamStages);
+    const int st = static_cast<int>(j % kStages);
     const uint32_t fb = smem_u32(&full[st]);
-    mbar_arrive_expect_tx(fb, kBlockBytes);
-    tma_load_2d(smem_u32(stage_data + st * (kBlock * kBlock)), &tmap_x, fb,
-                static_cast<int32_t>(bj * kBlock), static_cast<int32_t>(bi * kBlock));
+    mbar_arrive_expect_tx(fb, SC::kTileBytes);
+    tma_load_2d(smem_u32(stage_data + st * SC::kTileBytes), &tmap_x, fb, static_cast<int32_t>(bj * kBlock),
+                static_cast<int32_t>(bi * kBlock));
   };
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmap_x);
-    for (int j = 0; j < kStreamStages; ++j) issue(j);
+    for (int j = 0; j < kStages; ++j) issue(j);
   }
 
   int64_t j = 0;
   for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++j) {
-    const int st = static_cast<int>(j % kStreamStages);
-    const bool ok = mbar_wait(smem_u32(&full[st]), static_cast<uint32_t>((j / kStreamStages) & 1),
-                              abort_flag, status, limit_ns);
+    const int st = static_cast<int>(j % kStages);
+    const bool ok = mbar_wait(smem_u32(&full[st]), static_cast<uint32_t>((j / kStages) & 1), abort_flag,
+                              status, limit_ns);
     if (__syncthreads_or(!ok)) break;
     const int64_t bi = blk / blocks_per_row, bj = blk - bi * blocks_per_row;
-    const float* tile = stage_data + st * (kBlock * kBlock);
     float4 v[kRowsPerWarp];
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i)
-      v[i] = reinterpret_cast<const float4*>(tile + (warp * kRowsPerWarp + i) * kBlock)[lane];
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i)
-      m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
-    if (lane == 0) warp_amax[warp] = __uint_as_float(wmax);
-    __syncthreads();  // also: every thread has copied its part of the stage
-    // The stage is free again: refill it with the block kStreamStages ahead.
-    if (threadIdx.x == 0) issue(j + kStreamStages);
-    float amax = warp_amax[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, warp_amax[w]);
-    float s = amax / 448.0f;
-    if (s == 0.0f) s = 1.0f;
-    if constexpr (kPow2) s = pow2_round_up(s);
-    if (threadIdx.x == 0) scales[blk] = s;
-    const float r = 1.0f / s;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int tr = warp * kRowsPerWarp + i;
+      if constexpr (kBf16) {
+        const uint2 u = reinterpret_cast<const uint2*>(stage_data + st * SC::kTileBytes + tr * kBlock * 2)[lane];
+        v[i] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+      } else {
+        v[i] = reinterpret_cast<const float4*>(stage_data + st * SC::kTileBytes + tr * kBlock * 4)[lane];
+      }
+    }
     const int64_t r0 = bi * kBlock + warp * kRowsPerWarp;
     const int64_t c0 = bj * kBlock + lane * 4;
-    if constexpr (kPow2) {
-      encode_store<1, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
-    } else if (s >= 0x1p-126f) {
-      encode_store<0, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
+    if constexpr (kRowwise) {
+      __syncthreads();  // every thread has copied its part of the stage
+      if (threadIdx.x == 0) issue(j + kStages);
+      // Row maxima; lane i then computes row i's scale and its reciprocal (one
+      // division per warp instead of one per row), which the others read back.
+      float my_amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const float m =
+            fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+        const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
+        if (lane == i) my_amax = amax;
+      }
+      float my_s = my_amax / 448.0f;
+      if (my_s == 0.0f) my_s = 1.0f;
+      if constexpr (kPow2) my_s = pow2_round_up(my_s);
+      const float my_r = 1.0f / my_s;
+      if (lane < kRowsPerWarp && r0 + lane < rows) scales[(r0 + lane) * blocks_per_row + bj] = my_s;
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const float s = __shfl_sync(0xFFFFFFFFu, my_s, i);
+        const int64_t row = r0 + i;
+        if (row < rows) {
+          const float r = __shfl_sync(0xFFFFFFFFu, my_r, i);
+          uint32_t code;
+          if constexpr (kPow2) {
+            code = encode4<1>(v[i], s, r);
+          } else if (s >= 0x1p-126f) {
+            code = encode4<0>(v[i], s, r);
+          } else {
+            code = encode4<2>(v[i], s, r);
+          }
+          uint8_t* out = q + row * ld_q + c0;
+          if (c0 + 3 < cols) {
+            __stcs(reinterpret_cast<unsigned int*>(out), code);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              if (c0 + t < cols) out[t] = static_cast<uint8_t>((code >> (8 * t)) & 0xFFu);
+          }
+        }
+      }
     } else {
-      encode_store<2, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i)
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+      if (lane == 0) warp_amax[warp] = __uint_as_float(wmax);
+      __syncthreads();  // also: every thread has copied its part of the stage
+      // The stage is free again: refill it with the block kStages ahead.
+      if (threadIdx.x == 0) issue(j + kStages);
+      float amax = warp_amax[0];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, warp_amax[w]);
+      float s = amax / 448.0f;
+      if (s == 0.0f) s = 1.0f;
+      if constexpr (kPow2) s = pow2_round_up(s);
+      if (threadIdx.x == 0) scales[blk] = s;
+      const float r = 1.0f / s;
+      if constexpr (kPow2) {
+        encode_store<1, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
+      } else if (s >= 0x1p-126f) {
+        encode_store<0, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
+      } else {
+        encode_store<2, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
+      }
+      __syncthreads();  // warp_amax is rewritten by the next block
     }
-    __syncthreads();  // warp_amax is rewritten by the next block
   }
   // After a timeout, loads still in flight (blocks j .. issued-1) must land
   // before the CTA exits; each gets a bounded wait on its own phase.
   if (threadIdx.x == 0 && *abort_flag) {
     for (int64_t jj = j; jj < issued; ++jj) {
-      const uint32_t bar = smem_u32(&full[jj % kStreamStages]);
-      const uint32_t par = static_cast<uint32_t>((jj / kStreamStages) & 1);
+      const uint32_t bar = smem_u32(&full[jj % kStages]);
+      const uint32_t par = static_cast<uint32_t>((jj / kStages) & 1);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(bar, par)) {
         if (global_timer_ns() - t0 > 10000000ull) break;
@@ -277,7 +438,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Launch the streaming kernel (16-byte-aligned x, row stride a multiple of 16
+// bytes); false if the tensor map cannot be made (the caller falls back).
+template <bool kPow2, bool kRowwise, bool kBf16>
+bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q, int64_t ld_q,
+                   float* scales, cudaStream_t stream, cudaError_t& err) {
+  using SC = StreamCfg<kBf16>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return false;
+  CUtensorMap tm;
+  const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(ld_x) * SC::kElemBytes};
+  const uint32_t box[2] = {kBlock, kBlock};
+  if (!encode_tensor_map(&tm, kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, 2,
+                         dims, strides, box, false))
+    return false;
+  const size_t smem = 1024 + SC::kStages * SC::kTileBytes + SC::kStages * 8 + kWarps * 4 + 16;
+  auto kernel = quantize_stream_kernel<kPow2, kRowwise, kBf16>;
+  static std::atomic<uint64_t> attr_set{0};
+  if (!(attr_set.load() & (1ull << dev))) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+      err = cudaGetLastError();
+      return true;
+    }
+    attr_set.fetch_or(1ull << dev);
+  }
+  unsigned int* status = device_status_word();
+  if (!status) {
+    err = cudaErrorUnknown;
+    return true;
+  }
+  const int64_t nbr = (rows + kBlock - 1) / kBlock;
+  const int64_t nbc = (cols + kBlock - 1) / kBlock;
+  const int64_t nblocks = nbr * nbc;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, sms));
+  kernel<<<grid, kThreads, smem, stream>>>(tm, rows, cols, q, ld_q, scales, nbc, nblocks, status,
+                                           kDefaultWaitLimitNs);
+  err = cudaGetLastError();
+  return true;
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_1x128(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t ld_x,
+                                  uint8_t* q, int64_t ld_q, float* scales, bool pow2_scales,
+                                  cudaStream_t stream) {
+  const int64_t nbc = (cols + kBlock - 1) / kBlock;
+  const int64_t total = rows * nbc;
+  const int64_t esize = bf16 ? 2 : 4;
+  // TMA streaming when x is 16-byte aligned with a row stride that is a multiple of 16 bytes.
+  if (reinterpret_cast<uintptr_t>(x) % 16 == 0 && (ld_x * esize) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(q) % 4 == 0 && ld_q % 4 == 0) {
+    cudaError_t err = cudaSuccess;
+    bool done;
+    if (bf16)
+      done = pow2_scales ? launch_stream<true, true, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, true, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    else
+      done = pow2_scales ? launch_stream<true, true, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, true, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    if (done) return err;
+  }
+  const int64_t vbytes = 4 * esize;  // one lane's four elements
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % vbytes == 0) && ((ld_x * esize) % vbytes == 0) &&
+                   (reinterpret_cast<uintptr_t>(q) % 4 == 0) && (ld_q % 4 == 0);
+  int dev = 0;
+  int sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) sms = device_sm_count(dev);
+  if (sms <= 0) sms = 1;
+  // Enough warps to keep every SM's memory pipe busy, each with a contiguous run.
+  const int64_t max_blocks = static_cast<int64_t>(sms) * 8;
+  int64_t blocks = (total + k1xWarps * k1xSegs - 1) / (k1xWarps * k1xSegs);
+  blocks = std::max<int64_t>(1, std::min(blocks, max_blocks));
+  const int64_t warps = blocks * k1xWarps;
+  int64_t per_warp = (total + warps - 1) / warps;
+  per_warp = (per_warp + k1xSegs - 1) / k1xSegs * k1xSegs;
+  const dim3 grid(static_cast<unsigned>(blocks));
+#define DG_Q1X(BF, VEC, P2) \
+  quantize_1x128_kernel<BF, VEC, P2><<<grid, k1xThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc, per_warp)
+  if (bf16) {
+    if (vec) {
+      if (pow2_scales) DG_Q1X(true, true, true); else DG_Q1X(true, true, false);
+    } else {
+      if (pow2_scales) DG_Q1X(true, false, true); else DG_Q1X(true, false, false);
+    }
+  } else {
+    if (vec) {
+      if (pow2_scales) DG_Q1X(false, true, true); else DG_Q1X(false, true, false);
+    } else {
+      if (pow2_scales) DG_Q1X(false, false, true); else DG_Q1X(false, false, false);
+    }
+  }
+#undef DG_Q1X
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q,
                             int64_t ld_q, float* scales, bool pow2_scales, cudaStream_t stream) {
@@ -287,35 +544,12 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t 
   if (nblocks > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld_x % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(q) % 4 == 0) && (ld_q % 4 == 0);
-  int dev = 0;
-  if (vec && cudaGetDevice(&dev) == cudaSuccess) {
-    const int sms = device_sm_count(dev);
-    CUtensorMap tm;
-    const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(ld_x) * 4};
-    const uint32_t box[2] = {kBlock, kBlock};
-    if (sms > 0 && encode_tensor_map(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, 2, dims, strides, box, false)) {
-      const size_t smem = 1024 + kStreamStages * kBlockBytes + kStreamStages * 8 + kWarps * 4 + 16;
-      static std::atomic<uint64_t> attr_set{0};
-      if (dev < 64 && !(attr_set.load() & (1ull << dev))) {
-        if (cudaFuncSetAttribute(quantize_stream_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess ||
-            cudaFuncSetAttribute(quantize_stream_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-          return cudaGetLastError();
-        attr_set.fetch_or(1ull << dev);
-      }
-      unsigned int* status = device_status_word();
-      if (!status) return cudaGetLastError();
-      const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, sms));
-      if (pow2_scales)
-        quantize_stream_kernel<true><<<grid, kThreads, smem, stream>>>(tm, rows, cols, q, ld_q, scales, nbc,
-                                                                        nblocks, status, kDefaultWaitLimitNs);
-      else
-        quantize_stream_kernel<false><<<grid, kThreads, smem, stream>>>(tm, rows, cols, q, ld_q, scales, nbc,
-                                                                         nblocks, status, kDefaultWaitLimitNs);
-      return cudaGetLastError();
-    }
+  if (vec) {
+    cudaError_t err = cudaSuccess;
+    const bool done = pow2_scales
+                          ? launch_stream<true, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                          : launch_stream<false, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    if (done) return err;
   }
   const dim3 grid(static_cast<unsigned>(nblocks));
   if (vec) {

@@ -46,7 +46,7 @@ extern "C" {
 #define DG_API __attribute__((visibility("default")))
 #endif
 
-#define DG_ABI_VERSION 1u
+#define DG_ABI_VERSION 2u
 
 typedef enum {
     DG_OK = 0,
@@ -62,6 +62,12 @@ typedef enum {
     DG_SCALE_FP32 = 0,   /* scale = fl32(max|x| / 448); 1.0 for an all-zero block */
     DG_SCALE_UE8M0 = 1   /* the FP32 scale rounded up to a power of two, >= 2^-127 */
 } dg_scale_mode;
+
+/* Element type of a matrix handed to the row-wise quantizer. */
+typedef enum {
+    DG_INPUT_FP32 = 0,
+    DG_INPUT_BF16 = 1   /* raw 16-bit bfloat16 storage */
+} dg_input_dtype;
 
 /* ABI version of the loaded library (DG_ABI_VERSION at build time). */
 DG_API uint32_t dg_get_abi_version(void);
@@ -95,6 +101,23 @@ DG_API int dg_quantize_fp8_block(const float *x, int64_t rows, int64_t cols, int
                                  uint8_t *q, int64_t ld_q, float *scales,
                                  int scale_mode, void *stream);
 
+/* Row-wise quantizer: one scale per row and 128-column block, the per-token
+ * activation scaling that sits beside 128x128 weight scales (walkthrough §2.3:
+ * the block shape trades accuracy against overhead; pzsr.cn page §3.1). The
+ * steps are those of dg_quantize_fp8_block with blocks of 1 x 128.
+ *   x       [rows][ld_x] elements of x_dtype (a dg_input_dtype), finite values;
+ *           bfloat16 inputs are widened to FP32 exactly
+ *   q       [rows][ld_q] E4M3 codes out
+ *   scales  [rows][ceil(cols/128)] FP32 out
+ *   scale_mode  a dg_scale_mode
+ * rows == 0 or cols == 0 is a no-op. Needs ld_x >= cols and ld_q >= cols.
+ * Any alignment works; x 16-byte aligned with ld_x * element size a multiple
+ * of 16 bytes, and q 4-byte aligned with ld_q % 4 == 0, take the vectorized
+ * path. */
+DG_API int dg_quantize_fp8_1x128(const void *x, int x_dtype, int64_t rows, int64_t cols, int64_t ld_x,
+                                 uint8_t *q, int64_t ld_q, float *scales,
+                                 int scale_mode, void *stream);
+
 /* Dense NT GEMM (walkthrough §2.2, §3.2; pzsr.cn page §3.1, §4.1).
  *   c   [M][ld_c] bf16 out (raw 16-bit storage), rounded to nearest even
  *   a   [M][ld_a] E4M3 codes, K contiguous;  sa [ceil(M/128)][K/128] FP32
@@ -112,6 +135,18 @@ DG_API int dg_fp8_gemm_nt(void *c, int64_t ld_c,
                           const uint8_t *b, int64_t ld_b, const float *sb,
                           int64_t M, int64_t N, int64_t K,
                           int scale_mode, void *stream);
+
+/* Dense NT GEMM with one A scale per row and K block (row-wise activation
+ * scales from dg_quantize_fp8_1x128; pzsr.cn page §3.1): as dg_fp8_gemm_nt
+ * with
+ *   sa  [M][K/128] FP32: the scale of A[m, 128 kb .. 128 kb + 127]
+ * so that C[m, n] = bf16( sum_kb sa[m, kb] * sb[n/128, kb] * sum_{k in kb} A[m,k] B[n,k] ).
+ * Same size, stride and alignment rules as dg_fp8_gemm_nt. */
+DG_API int dg_fp8_gemm_nt_1x128(void *c, int64_t ld_c,
+                                const uint8_t *a, int64_t ld_a, const float *sa,
+                                const uint8_t *b, int64_t ld_b, const float *sb,
+                                int64_t M, int64_t N, int64_t K,
+                                int scale_mode, void *stream);
 
 /* M-grouped contiguous GEMM for MoE experts (pzsr.cn page §2.3, §3.2, §3.3).
  *   c          [M_tot][ld_c] bf16 out
@@ -131,6 +166,15 @@ DG_API int dg_fp8_grouped_gemm_contiguous(void *c, int64_t ld_c,
                                           const int32_t *m_indices,
                                           int64_t M_tot, int64_t N, int64_t K,
                                           int scale_mode, void *stream);
+
+/* M-grouped contiguous GEMM with one A scale per row and K block:
+ * as dg_fp8_grouped_gemm_contiguous with sa [M_tot][K/128] FP32. */
+DG_API int dg_fp8_grouped_gemm_contiguous_1x128(void *c, int64_t ld_c,
+                                                const uint8_t *a, int64_t ld_a, const float *sa,
+                                                const uint8_t *b, const float *sb, int num_groups,
+                                                const int32_t *m_indices,
+                                                int64_t M_tot, int64_t N, int64_t K,
+                                                int scale_mode, void *stream);
 
 /* Synchronize `stream`, then read and clear the current device's status word.
  * Returns DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_strings_alignment(L):
-    assert bq.dg_get_abi_version() == 1
+    assert bq.dg_get_abi_version() == 2
     assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
     for s in range(7):
         assert bq.dg_status_string(s)
@@ -55,6 +55,25 @@ def grouped(L, c=P, ldc=256, a=P, lda=512, sa=P, b=P, sb=P, g=2, mi=P, m=256, n=
 
 def quant(L, x=P, rows=128, cols=128, ldx=128, q=P, ldq=128, s=P, mode=0):
     return L.dg_quantize_fp8_block(x, rows, cols, ldx, q, ldq, s, mode, None)
+
+
+def quant_rows(L, x=P, dtype=0, rows=128, cols=128, ldx=128, q=P, ldq=128, s=P, mode=0):
+    return L.dg_quantize_fp8_1x128(x, dtype, rows, cols, ldx, q, ldq, s, mode, None)
+
+
+def gemm_rows(L, **kw):
+    a = dict(c=P, ldc=256, a=P, lda=512, sa=P, b=P, ldb=512, sb=P, m=128, n=256, k=512, mode=0)
+    a.update(kw)
+    return L.dg_fp8_gemm_nt_1x128(a["c"], a["ldc"], a["a"], a["lda"], a["sa"], a["b"], a["ldb"], a["sb"],
+                                  a["m"], a["n"], a["k"], a["mode"], None)
+
+
+def grouped_rows(L, **kw):
+    a = dict(c=P, ldc=256, a=P, lda=512, sa=P, b=P, sb=P, g=2, mi=P, m=256, n=256, k=512, mode=0)
+    a.update(kw)
+    return L.dg_fp8_grouped_gemm_contiguous_1x128(a["c"], a["ldc"], a["a"], a["lda"], a["sa"], a["b"],
+                                                  a["sb"], a["g"], a["mi"], a["m"], a["n"], a["k"],
+                                                  a["mode"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -91,11 +110,44 @@ def test_quantize_argument_errors(L, kw, status):
     assert quant(L, **kw) == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=NULL), bq.DG_ERR_INVALID_ARG), (dict(q=NULL), bq.DG_ERR_INVALID_ARG),
+    (dict(dtype=2), bq.DG_ERR_INVALID_ARG), (dict(mode=3), bq.DG_ERR_INVALID_ARG),
+    (dict(cols=-5), bq.DG_ERR_INVALID_ARG), (dict(ldx=64), bq.DG_ERR_INVALID_ARG),
+    (dict(x=P + 2), bq.DG_ERR_MISALIGNED), (dict(x=P + 1, dtype=1), bq.DG_ERR_MISALIGNED),
+    (dict(s=P + 2), bq.DG_ERR_MISALIGNED), (dict(rows=0), bq.DG_OK), (dict(cols=0, x=NULL), bq.DG_OK),
+])
+def test_rowwise_quantize_argument_errors(L, kw, status):
+    assert quant_rows(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(sa=NULL), bq.DG_ERR_INVALID_ARG), (dict(mode=5), bq.DG_ERR_INVALID_ARG),
+    (dict(k=500), bq.DG_ERR_UNSUPPORTED_SHAPE), (dict(a=P + 8), bq.DG_ERR_MISALIGNED),
+    (dict(m=0), bq.DG_OK),
+])
+def test_rowwise_gemm_argument_errors(L, kw, status):
+    assert gemm_rows(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(sa=NULL), bq.DG_ERR_INVALID_ARG), (dict(mi=NULL), bq.DG_ERR_INVALID_ARG),
+    (dict(m=200), bq.DG_ERR_UNSUPPORTED_SHAPE), (dict(mi=P + 4), bq.DG_ERR_MISALIGNED),
+    (dict(m=0), bq.DG_OK),
+])
+def test_rowwise_grouped_argument_errors(L, kw, status):
+    assert grouped_rows(L, **kw) == status
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_arguments_without_gpu_report_no_device(L):
     assert gemm(L) == bq.DG_ERR_NO_DEVICE
     assert grouped(L) == bq.DG_ERR_NO_DEVICE
     assert quant(L) == bq.DG_ERR_NO_DEVICE
+    assert quant_rows(L) == bq.DG_ERR_NO_DEVICE
+    assert quant_rows(L, dtype=1) == bq.DG_ERR_NO_DEVICE
+    assert gemm_rows(L) == bq.DG_ERR_NO_DEVICE
+    assert grouped_rows(L) == bq.DG_ERR_NO_DEVICE
     assert L.dg_selftest_wait_timeout(1000, None) == bq.DG_ERR_NO_DEVICE
 
 
