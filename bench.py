@@ -343,7 +343,7 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------------------------
-# Auxiliary workloads (profiling and per-config sweeps; not the contract line).
+# Auxiliary workloads (profiling and per-workload sweeps; not the contract line).
 # Memory-bound cases rotate through enough input copies that every launch reads
 # HBM, not a warm L2 (working set >= 3x the 129 MB L2).
 # ------------------------------------------------------------------------------

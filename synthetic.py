@@ -32,9 +32,9 @@ MOE = dict(experts=8, tokens=4096, topk=2, hidden=4096, intermediate=11008)
 SQUARES = (4096, 8192, 16384)
 
 
-def seed_for(config: int, index: int = 0) -> int:
-    """Seed of shape `index` of workload `config` (1000 * config + index)."""
-    return 1000 * int(config) + int(index)
+def seed_for(workload: int, index: int = 0) -> int:
+    """Seed of shape `index` of numbered workload `workload` (1000 * workload + index)."""
+    return 1000 * int(workload) + int(index)
 
 
 def normal(shape, seed: int) -> np.ndarray:

@@ -61,8 +61,8 @@ def test_quantize_unaligned_and_strided(oracle_mod, dtype):
     assert np.array_equal(s2, sr2) and np.array_equal(q2, qr2)
 
 
-def test_quantize_config_size_sampled_rows(oracle_mod):
-    """The config-3 activation size, 16384 x 7168 FP32, checked on sampled rows."""
+def test_quantize_16384x7168_sampled_rows(oracle_mod):
+    """The benchmark activation size, 16384 x 7168 FP32, checked on sampled rows."""
     r, c = synthetic.QUANT_SHAPE
     x = synthetic.normal((r, c), seed=synthetic.seed_for(3, 99))
     q, s = _gpu_quant(to_dev(x, device()), 0)

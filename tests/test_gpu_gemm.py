@@ -43,7 +43,7 @@ def _check(oracle_mod, qa, sa, qb, sb, rows=None, mode=0, what=""):
     return assert_within_bound(got, ref, mag, what)
 
 
-def test_tiny_config(oracle_mod):
+def test_tiny_128x256x512(oracle_mod):
     m, n, k = synthetic.TINY
     qa, sa, qb, sb = _operands(oracle_mod, m, n, k, synthetic.seed_for(1))
     _check(oracle_mod, qa, sa, qb, sb, what="128x256x512")

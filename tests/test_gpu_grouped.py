@@ -61,7 +61,7 @@ def test_small_groups_with_empty_expert_and_padding(oracle_mod, mode):
     assert torch.count_nonzero(c[torch.as_tensor(m_idx < 0, device=c.device)]) == 0
 
 
-def test_moe_config(oracle_mod):
+def test_moe_8_experts_11008x4096(oracle_mod):
     """8 experts, K = 4096 hidden, N = 11008 intermediate, 4096 tokens top-2."""
     mo = synthetic.MOE
     a, b, m_idx, sizes = synthetic.moe_inputs(seed=0, experts=mo["experts"], tokens=mo["tokens"],
