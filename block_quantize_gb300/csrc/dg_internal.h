@@ -5,8 +5,40 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace dg {
+
+// Launch a kernel with programmatic dependent launch allowed (and a cluster
+// of cluster_x CTAs when cluster_x > 0). The kernel may then begin while the
+// previous work on the stream finishes, so it must execute griddepcontrol.wait
+// (pdl_wait) before it touches global memory; our kernels do that right after
+// their set-up (barriers, TMEM, tensor-map prefetch) and then let the next
+// launch begin (pdl_trigger).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // 128x128 block quantizer launch (sizes already validated, rows, cols > 0).
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld_x,

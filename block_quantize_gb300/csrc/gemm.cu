@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
 
   const int num_tiles = args.num_mb * args.num_nb;
   uint32_t loads_issued = 0;  // producer: K-block loads issued
@@ -675,8 +677,11 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
   if (p.num_sms_cap > 0) grid = std::min(grid, p.num_sms_cap);
   grid = std::max(grid, 1);
-  kernel<<<grid, Cf::kThreads, smem, stream>>>(ta, tb, tc, args);
-  return cudaGetLastError() == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+  if (launch_kernel(kernel, dim3(grid), dim3(Cf::kThreads), smem, stream, 0, ta, tb, tc, args) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  return DG_OK;
 }
 
 }  // namespace

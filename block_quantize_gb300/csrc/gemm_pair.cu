@@ -253,6 +253,8 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
   tc_fence_after();
   cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or load
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
   const int num_tiles = args.num_pm * args.num_nb;
   uint32_t loads_issued = 0;
 
@@ -495,6 +497,8 @@ __global__ void __launch_bounds__(kNatThreads, 1)
   tc_fence_after();
   cluster_sync_all();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
   const int num_tiles = args.num_pm * args.num_nb;
   uint32_t loads_issued = 0;
 
@@ -832,19 +836,8 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
       return DG_ERR_CUDA;
   }
 
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kind.threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kind.kernel, ta, tb, tc, args) != cudaSuccess) {
+  if (launch_kernel(kind.kernel, dim3(2 * pairs), dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args) !=
+      cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }

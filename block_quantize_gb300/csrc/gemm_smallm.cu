@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   tc_fence_after();
   cluster_sync_all();  // every peer's barriers exist before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
   uint32_t loads_issued = 0;
 
   if (warp == 0) {
@@ -498,19 +500,8 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
     if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
       return DG_ERR_CUDA;
   }
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = args.split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(args.split * args.num_clusters, 1, 1);
-  cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, fp8_gemm_splitk_kernel<BN>, ta, tb, args) != cudaSuccess) {
+  if (launch_kernel(fp8_gemm_splitk_kernel<BN>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
+                    smem, stream, static_cast<unsigned>(args.split), ta, tb, args) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }

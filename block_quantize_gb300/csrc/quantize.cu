@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
                                                             float* __restrict__ scales,
                                                             int64_t blocks_per_row) {
   __shared__ float warp_amax[kWarps];
+  pdl_wait();
+  pdl_trigger();
   const int64_t blk = blockIdx.x;
   const int64_t bi = blk / blocks_per_row;
   const int64_t bj = blk - bi * blocks_per_row;
@@ -228,6 +230,8 @@ template <bool kBf16, bool kVec, bool kPow2>
 __global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
     const void* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* __restrict__ q, int64_t ld_q,
     float* __restrict__ scales, int64_t nbc, int64_t per_warp) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t w = static_cast<int64_t>(blockIdx.x) * k1xWarps + (threadIdx.x >> 5);
   const int64_t total = rows * nbc;
@@ -315,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   int64_t issued = 0;  // thread 0: blocks whose load was issued (in order)
   auto issue = [&](int64_t j) {  // load this CTA's j-th block into stage j % kStages
@@ -475,9 +481,9 @@ bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint
   const int64_t nbc = (cols + kBlock - 1) / kBlock;
   const int64_t nblocks = nbr * nbc;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, sms));
-  kernel<<<grid, kThreads, smem, stream>>>(tm, rows, cols, q, ld_q, scales, nbc, nblocks, status,
-                                           kDefaultWaitLimitNs);
-  err = cudaGetLastError();
+  err = launch_kernel(kernel, dim3(grid), dim3(kThreads), smem, stream, 0, tm, rows, cols, q, ld_q, scales, nbc,
+                      nblocks, status, kDefaultWaitLimitNs);
+  if (err != cudaSuccess) cudaGetLastError();
   return true;
 }
 
@@ -517,8 +523,10 @@ cudaError_t launch_quantize_1x128(const void* x, bool bf16, int64_t rows, int64_
   int64_t per_warp = (total + warps - 1) / warps;
   per_warp = (per_warp + k1xSegs - 1) / k1xSegs * k1xSegs;
   const dim3 grid(static_cast<unsigned>(blocks));
-#define DG_Q1X(BF, VEC, P2) \
-  quantize_1x128_kernel<BF, VEC, P2><<<grid, k1xThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc, per_warp)
+  cudaError_t err = cudaSuccess;
+#define DG_Q1X(BF, VEC, P2)                                                                                \
+  err = launch_kernel(quantize_1x128_kernel<BF, VEC, P2>, grid, dim3(k1xThreads), 0, stream, 0, x, rows, cols, \
+                      ld_x, q, ld_q, scales, nbc, per_warp)
   if (bf16) {
     if (vec) {
       if (pow2_scales) DG_Q1X(true, true, true); else DG_Q1X(true, true, false);
@@ -533,7 +541,8 @@ cudaError_t launch_quantize_1x128(const void* x, bool bf16, int64_t rows, int64_
     }
   }
 #undef DG_Q1X
-  return cudaGetLastError();
+  if (err != cudaSuccess) cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q,
@@ -552,18 +561,12 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t 
     if (done) return err;
   }
   const dim3 grid(static_cast<unsigned>(nblocks));
-  if (vec) {
-    if (pow2_scales)
-      quantize_kernel<true, true><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc);
-    else
-      quantize_kernel<true, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc);
-  } else {
-    if (pow2_scales)
-      quantize_kernel<false, true><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc);
-    else
-      quantize_kernel<false, false><<<grid, kThreads, 0, stream>>>(x, rows, cols, ld_x, q, ld_q, scales, nbc);
-  }
-  return cudaGetLastError();
+  auto kernel = vec ? (pow2_scales ? quantize_kernel<true, true> : quantize_kernel<true, false>)
+                    : (pow2_scales ? quantize_kernel<false, true> : quantize_kernel<false, false>);
+  const cudaError_t err = launch_kernel(kernel, grid, dim3(kThreads), 0, stream, 0, x, rows, cols, ld_x, q, ld_q,
+                                        scales, nbc);
+  if (err != cudaSuccess) cudaGetLastError();
+  return err;
 }
 
 }  // namespace dg
