@@ -308,10 +308,10 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
           reinterpret_cast<float4*>(prow)[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
       }
-      // The warp's writes are ordered before lane 0's releasing remote arrives.
+      // The warp's writes are ordered (warp barrier) before the releasing remote
+      // arrives; lane s signals peer s, so the arrives to all peers overlap.
       __syncwarp();
-      if (lane == 0)
-        for (int s = 0; s < split; ++s) mbar_arrive_remote(mapa_shared(smem_u32(ready_bar), s));
+      if (lane < split) mbar_arrive_remote(mapa_shared(smem_u32(ready_bar), lane));
 
       // Reduce this CTA's columns over the cluster's partials, in rank order.
       {
@@ -338,8 +338,7 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
                      make_float2(sum[4], sum[5]), make_float2(sum[6], sum[7]));
       }
       __syncwarp();
-      if (lane == 0)
-        for (int s = 0; s < split; ++s) mbar_arrive_remote(mapa_shared(smem_u32(consumed_bar), s));
+      if (lane < split) mbar_arrive_remote(mapa_shared(smem_u32(consumed_bar), lane));
     }
     __syncwarp();
   }
