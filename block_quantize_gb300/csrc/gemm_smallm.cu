@@ -435,8 +435,8 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
 
   // Model (measured on GB300 with TMA streams of 128-byte rows): one SM
   // streams ~45 GB/s; all SMs together ~4.8 TB/s with 128-row boxes and
-  // ~5.4 TB/s with 256-row boxes; a cluster reduction costs ~2 us per tile
-  // (mostly waiting for the slowest peer). Time = max(whole-GPU stream of B,
+  // ~5.4 TB/s with 256-row boxes; a cluster reduction costs ~1 us per tile
+  // (mostly waiting for the slowest peer; measured, then swept). Time = max(whole-GPU stream of B,
   // the slowest cluster's K range per tile + its reductions).
   const double sm_bytes_per_us = 4.5e4;
   const double gpu_bytes_per_us = (BN == 256) ? 5.4e6 : 4.8e6;
@@ -451,7 +451,7 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
     const int waves = (args.num_nb + clusters - 1) / clusters;
     const int kbs = (args.num_kb + split - 1) / split;
     const double per_cluster =
-        waves * (kbs * static_cast<double>(C::kBTileBytes) / sm_bytes_per_us + (split > 1 ? 2.0 : 0.0));
+        waves * (kbs * static_cast<double>(C::kBTileBytes) / sm_bytes_per_us + (split > 1 ? 1.0 : 0.0));
     const double cost = std::max(b_bytes / gpu_bytes_per_us, per_cluster) * (1.0 + 0.01 * split);
     if (cost < plan.cost) {
       plan.cost = cost;
