@@ -508,6 +508,37 @@ def run_aux(args):
         tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
         out["results"] = [{"M": m, "N": n, "K": k, "us": ms * 1e3, "tflops": tf,
                            "frac_fp8_burst": tf / fp8_peak}]
+    elif kind == "requant":
+        # GEMM with the output requantized in the epilogue (E4M3 + scales), against
+        # the bf16 GEMM and the unfused chain bf16 GEMM -> row-wise quantizer.
+        dims, _, only = (spec or "4096,7168,2048").partition(":")
+        m, n, k = (int(v) for v in dims.split(","))
+        qa, sa = _rand_fp8((m, k), dev, gen, 0)
+        copies = max(1, -(-3 * L2_BYTES // (n * k)))
+        bs = [_rand_fp8((n, k), dev, gen, 0) for _ in range(copies)]
+        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        cq = torch.empty((m, n), dtype=torch.uint8, device=dev)
+        cs_row = torch.empty((m, -(-n // 128)), dtype=torch.float32, device=dev)
+        cs_blk = torch.empty((-(-m // 128), -(-n // 128)), dtype=torch.float32, device=dev)
+        variants = {
+            "bf16": [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb) for qb, sb in bs],
+            "requant_1x128": [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt_requant(qa, qb, sa, sb, 0, 1, 0, cq, cs_row)
+                              for qb, sb in bs],
+            "requant_128x128": [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt_requant(qa, qb, sa, sb, 0, 128, 0, cq, cs_blk)
+                                for qb, sb in bs],
+            "bf16_then_quantize_1x128": [
+                lambda qb=qb, sb=sb: (bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb), bq.dg_quantize_fp8_1x128(c, 0, cq, cs_row))
+                for qb, sb in bs],
+        }
+        res = []
+        for name, fns in variants.items():
+            if only and name != only:
+                continue
+            ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+            tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+            res.append({"variant": name, "M": m, "N": n, "K": k, "us": ms * 1e3, "tflops": tf,
+                        "frac_fp8_burst": tf / fp8_peak})
+        out["results"] = res
     elif kind == "grouped":
         mo = synthetic.MOE
         sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
@@ -544,7 +575,8 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
-                        "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K]  "
+                        "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K] | "
+                        "requant[:M,N,K[:variant]]  "
                         "(the others print per-kernel numbers for profiling)")
     args = p.parse_args()
     if args.steps is None:

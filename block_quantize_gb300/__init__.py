@@ -14,6 +14,9 @@ The three compute calls carry the C names:
   pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析" §4.1.
 * ``dg_fp8_grouped_gemm_contiguous(c, a, b, sa, sb, m_indices, scale_mode)``:
   the M-grouped contiguous MoE variant (same page §2.3, §3.2).
+* ``dg_fp8_gemm_nt_requant`` / ``dg_fp8_grouped_gemm_contiguous_requant``: the
+  same GEMMs with the FP32 accumulators requantized to E4M3 codes plus block
+  scales in the epilogue (walkthrough §2.2, §6); they return ``(cq, cs)``.
 """
 from __future__ import annotations
 
@@ -30,6 +33,8 @@ __all__ = [
     "dg_get_abi_version", "dg_status_string", "dg_get_mk_alignment_for_contiguous_layout",
     "dg_set_num_sms", "dg_get_num_sms", "dg_quantize_fp8_block", "dg_fp8_gemm_nt",
     "dg_fp8_grouped_gemm_contiguous", "dg_get_device_status", "dg_selftest_wait_timeout",
+    "dg_quantize_fp8_1x128", "dg_fp8_gemm_nt_1x128", "dg_fp8_grouped_gemm_contiguous_1x128",
+    "dg_fp8_gemm_nt_requant", "dg_fp8_grouped_gemm_contiguous_requant",
     "declared_functions",
 ]
 
@@ -95,6 +100,12 @@ def lib() -> ctypes.CDLL:
         L.dg_fp8_gemm_nt_1x128.restype = i32
         L.dg_fp8_grouped_gemm_contiguous_1x128.argtypes = L.dg_fp8_grouped_gemm_contiguous.argtypes
         L.dg_fp8_grouped_gemm_contiguous_1x128.restype = i32
+        L.dg_fp8_gemm_nt_requant.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, i32, vp, i64, vp,
+                                             i64, i64, i64, i32, vp]
+        L.dg_fp8_gemm_nt_requant.restype = i32
+        L.dg_fp8_grouped_gemm_contiguous_requant.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, i32, vp, vp,
+                                                             i32, vp, i64, i64, i64, i32, vp]
+        L.dg_fp8_grouped_gemm_contiguous_requant.restype = i32
         L.dg_get_device_status.argtypes = [vp]
         L.dg_get_device_status.restype = i32
         L.dg_selftest_wait_timeout.argtypes = [i64, vp]
@@ -290,6 +301,104 @@ def _grouped(c, a, b, sa, sb, m_indices, scale_mode, a_1x128):
         m_tot, n, k, int(scale_mode), _stream(c))
     _check(st, "dg_fp8_grouped_gemm_contiguous_1x128" if a_1x128 else "dg_fp8_grouped_gemm_contiguous")
     return c
+
+
+def _requant_out(cq, cs, m, n, out_block_rows, device):
+    """Output tensors of a requantizing GEMM: codes [m, n] (row stride a
+    multiple of 16) and scales [m or ceil(m/128), ceil(n/128)]."""
+    if out_block_rows not in (1, BLOCK):
+        raise ValueError("out_block_rows must be 1 or 128")
+    nbc = (n + BLOCK - 1) // BLOCK
+    s_rows = m if out_block_rows == 1 else (m + BLOCK - 1) // BLOCK
+    if cq is None:
+        ld = max(16, (n + 15) // 16 * 16)
+        cq = torch.empty((m, ld), dtype=torch.uint8, device=device)[:, :n]
+    if cs is None:
+        cs = torch.empty((s_rows, nbc), dtype=torch.float32, device=device)
+    qb = _u8(cq)
+    _cuda(qb, torch.uint8, "cq")
+    _cuda(cs, torch.float32, "cs")
+    if tuple(qb.shape) != (m, n):
+        raise ValueError("cq shape mismatch")
+    if tuple(cs.shape) != (s_rows, nbc) or not cs.is_contiguous():
+        raise ValueError(f"cs must be a contiguous [{s_rows}, {nbc}] tensor")
+    return cq, qb, cs
+
+
+def dg_fp8_gemm_nt_requant(a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,
+                           scale_mode: int = DG_SCALE_FP32, out_block_rows: int = 1,
+                           out_scale_mode: int = DG_SCALE_FP32, cq: torch.Tensor | None = None,
+                           cs: torch.Tensor | None = None):
+    """Block-scaled A[M, K] . B[N, K]^T with the FP32 result requantized to
+    E4M3 in the epilogue: returns (cq uint8 [M, N], cs float32) with one scale
+    per out_block_rows x 128 block. sa is [ceil(M/128), K/128] or, for
+    row-wise activation scales, [M, K/128]."""
+    a, b = _u8(a), _u8(b)
+    _cuda(a, torch.uint8, "a")
+    _cuda(b, torch.uint8, "b")
+    _cuda(sa, torch.float32, "sa")
+    _cuda(sb, torch.float32, "sb")
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k:
+        raise ValueError("shape mismatch between a and b")
+    kb = k // BLOCK
+    if tuple(sa.shape) == (m, kb) and m != (m + BLOCK - 1) // BLOCK:
+        a_scale_rows = 1
+    elif tuple(sa.shape) == ((m + BLOCK - 1) // BLOCK, kb):
+        a_scale_rows = BLOCK
+    else:
+        raise ValueError("sa must be [ceil(M/128), K/128] or [M, K/128]")
+    if tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
+        raise ValueError("scale shape mismatch")
+    if not (sa.is_contiguous() and sb.is_contiguous()):
+        raise ValueError("scales must be contiguous")
+    cq, qb, cs = _requant_out(cq, cs, m, n, out_block_rows, a.device)
+    st = lib().dg_fp8_gemm_nt_requant(
+        ctypes.c_void_p(qb.data_ptr()), _ld(qb, "cq"), ctypes.c_void_p(cs.data_ptr()), int(out_block_rows),
+        int(out_scale_mode), ctypes.c_void_p(a.data_ptr()), _ld(a, "a"), ctypes.c_void_p(sa.data_ptr()),
+        a_scale_rows, ctypes.c_void_p(b.data_ptr()), _ld(b, "b"), ctypes.c_void_p(sb.data_ptr()),
+        m, n, k, int(scale_mode), _stream(a))
+    _check(st, "dg_fp8_gemm_nt_requant")
+    return cq, cs
+
+
+def dg_fp8_grouped_gemm_contiguous_requant(a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor,
+                                           sb: torch.Tensor, m_indices: torch.Tensor,
+                                           scale_mode: int = DG_SCALE_FP32, out_block_rows: int = 1,
+                                           out_scale_mode: int = DG_SCALE_FP32,
+                                           cq: torch.Tensor | None = None, cs: torch.Tensor | None = None):
+    """The M-grouped contiguous GEMM with its output requantized to E4M3
+    (padding rows: codes 0); returns (cq, cs) as dg_fp8_gemm_nt_requant."""
+    a, b = _u8(a), _u8(b)
+    _cuda(a, torch.uint8, "a")
+    _cuda(b, torch.uint8, "b")
+    _cuda(sa, torch.float32, "sa")
+    _cuda(sb, torch.float32, "sb")
+    _cuda(m_indices, torch.int32, "m_indices")
+    m_tot, k = a.shape
+    g, n, k2 = b.shape
+    if k2 != k or tuple(m_indices.shape) != (m_tot,):
+        raise ValueError("shape mismatch")
+    kb = k // BLOCK
+    if tuple(sa.shape) == (m_tot, kb) and m_tot != (m_tot + BLOCK - 1) // BLOCK:
+        a_scale_rows = 1
+    elif tuple(sa.shape) == ((m_tot + BLOCK - 1) // BLOCK, kb):
+        a_scale_rows = BLOCK
+    else:
+        raise ValueError("sa must be [M_tot/128, K/128] or [M_tot, K/128]")
+    if tuple(sb.shape) != (g, (n + BLOCK - 1) // BLOCK, kb):
+        raise ValueError("scale shape mismatch")
+    if not (b.is_contiguous() and sa.is_contiguous() and sb.is_contiguous() and m_indices.is_contiguous()):
+        raise ValueError("b, sa, sb and m_indices must be contiguous")
+    cq, qb, cs = _requant_out(cq, cs, m_tot, n, out_block_rows, a.device)
+    st = lib().dg_fp8_grouped_gemm_contiguous_requant(
+        ctypes.c_void_p(qb.data_ptr()), _ld(qb, "cq"), ctypes.c_void_p(cs.data_ptr()), int(out_block_rows),
+        int(out_scale_mode), ctypes.c_void_p(a.data_ptr()), _ld(a, "a"), ctypes.c_void_p(sa.data_ptr()),
+        a_scale_rows, ctypes.c_void_p(b.data_ptr()), ctypes.c_void_p(sb.data_ptr()), g,
+        ctypes.c_void_p(m_indices.data_ptr()), m_tot, n, k, int(scale_mode), _stream(a))
+    _check(st, "dg_fp8_grouped_gemm_contiguous_requant")
+    return cq, cs
 
 
 def dg_get_device_status(device=None) -> int:

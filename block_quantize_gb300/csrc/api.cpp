@@ -77,6 +77,46 @@ int zero_output(void* c, int64_t ld_c, int64_t M, int64_t N, cudaStream_t st) {
   return DG_OK;
 }
 
+// Checks the E4M3 output arguments of a requantizing GEMM (after the common
+// checks, which have already applied the bf16 rules to q and ld_q).
+int validate_requant_out(const uint8_t* q, int64_t ld_q, const float* s, int out_block_rows,
+                         int out_scale_mode, int a_scale_rows) {
+  if (out_block_rows != 1 && out_block_rows != 128) return DG_ERR_INVALID_ARG;
+  if (a_scale_rows != 1 && a_scale_rows != 128) return DG_ERR_INVALID_ARG;
+  if (out_scale_mode != DG_SCALE_FP32 && out_scale_mode != DG_SCALE_UE8M0) return DG_ERR_INVALID_ARG;
+  if (!q || !s) return DG_ERR_INVALID_ARG;
+  if (!aligned(s, 4)) return DG_ERR_MISALIGNED;
+  if (!aligned(q, 16) || ld_q % 16 != 0) return DG_ERR_MISALIGNED;
+  return DG_OK;
+}
+
+// Requantized C = 0 when the K extent is empty: codes 0, every scale 1.
+int zero_requant_output(const dg::RequantOut& o, int64_t M, int64_t N, cudaStream_t st) {
+  if (cudaMemset2DAsync(o.q, static_cast<size_t>(o.ld_q), 0, static_cast<size_t>(N), static_cast<size_t>(M),
+                        st) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  const int64_t rows = o.block_rows == 1 ? M : (M + 127) / 128;
+  if (dg::launch_fill_f32(o.s, rows * o.ld_s, 1.0f, st) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  return DG_OK;
+}
+
+dg::RequantOut make_requant(uint8_t* q, int64_t ld_q, float* s, int out_block_rows, int out_scale_mode,
+                            int64_t N) {
+  dg::RequantOut o{};
+  o.q = q;
+  o.ld_q = ld_q;
+  o.s = s;
+  o.ld_s = (N + 127) / 128;
+  o.block_rows = out_block_rows;
+  o.pow2 = out_scale_mode == DG_SCALE_UE8M0 ? 1 : 0;
+  return o;
+}
+
 }  // namespace
 
 extern "C" {
@@ -142,17 +182,19 @@ DG_API int dg_quantize_fp8_1x128(const void* x, int x_dtype, int64_t rows, int64
   return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
+// rq.q != nullptr: E4M3 output (c and ld_c then describe the codes).
 static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                       const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
-                      int scale_mode, void* stream, bool a_1x128) {
+                      int scale_mode, void* stream, bool a_1x128, const dg::RequantOut& rq) {
   const int v = validate_gemm_common(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode);
   if (v == kEmpty) return DG_OK;
   if (v != DG_OK) return v;
   const int dev_st = check_device();
   if (dev_st != DG_OK) return dev_st;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(c, ld_c, M, N, st);
+  if (K == 0) return rq.q ? zero_requant_output(rq, M, N, st) : zero_output(c, ld_c, M, N, st);
   dg::GemmProblem p{};
+  p.rq = rq;
   p.c = c;
   p.ld_c = ld_c;
   p.a = a;
@@ -175,18 +217,33 @@ static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, con
 DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                           const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
                           int64_t K, int scale_mode, void* stream) {
-  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, false);
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, false, dg::RequantOut{});
 }
 
 DG_API int dg_fp8_gemm_nt_1x128(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                                 const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
                                 int64_t K, int scale_mode, void* stream) {
-  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, true);
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, true, dg::RequantOut{});
+}
+
+DG_API int dg_fp8_gemm_nt_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_block_rows, int out_scale_mode,
+                                  const uint8_t* a, int64_t ld_a, const float* sa, int a_scale_rows,
+                                  const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
+                                  int64_t K, int scale_mode, void* stream) {
+  if (M > 0 && N > 0) {
+    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
+    if (v != DG_OK) return v;
+  } else if (out_block_rows != 1 && out_block_rows != 128) {
+    return DG_ERR_INVALID_ARG;
+  }
+  return gemm_dense(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, a_scale_rows == 1,
+                    make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
 }
 
 static int gemm_grouped(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                         const uint8_t* b, const float* sb, int num_groups, const int32_t* m_indices,
-                        int64_t M_tot, int64_t N, int64_t K, int scale_mode, void* stream, bool a_1x128) {
+                        int64_t M_tot, int64_t N, int64_t K, int scale_mode, void* stream, bool a_1x128,
+                        const dg::RequantOut& rq) {
   const int v = validate_gemm_common(c, ld_c, a, ld_a, sa, b, K, sb, M_tot, N, K, scale_mode);
   if (v == kEmpty) return (num_groups < 1 || M_tot % 128 != 0) ? DG_ERR_INVALID_ARG : DG_OK;
   if (v != DG_OK) return v;
@@ -197,8 +254,9 @@ static int gemm_grouped(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, c
   const int dev_st = check_device();
   if (dev_st != DG_OK) return dev_st;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(c, ld_c, M_tot, N, st);
+  if (K == 0) return rq.q ? zero_requant_output(rq, M_tot, N, st) : zero_output(c, ld_c, M_tot, N, st);
   dg::GemmProblem p{};
+  p.rq = rq;
   p.c = c;
   p.ld_c = ld_c;
   p.a = a;
@@ -223,7 +281,7 @@ DG_API int dg_fp8_grouped_gemm_contiguous(void* c, int64_t ld_c, const uint8_t* 
                                           int num_groups, const int32_t* m_indices, int64_t M_tot,
                                           int64_t N, int64_t K, int scale_mode, void* stream) {
   return gemm_grouped(c, ld_c, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
-                      false);
+                      false, dg::RequantOut{});
 }
 
 DG_API int dg_fp8_grouped_gemm_contiguous_1x128(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a,
@@ -231,7 +289,23 @@ DG_API int dg_fp8_grouped_gemm_contiguous_1x128(void* c, int64_t ld_c, const uin
                                                 int num_groups, const int32_t* m_indices, int64_t M_tot,
                                                 int64_t N, int64_t K, int scale_mode, void* stream) {
   return gemm_grouped(c, ld_c, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
-                      true);
+                      true, dg::RequantOut{});
+}
+
+DG_API int dg_fp8_grouped_gemm_contiguous_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_block_rows,
+                                                  int out_scale_mode, const uint8_t* a, int64_t ld_a,
+                                                  const float* sa, int a_scale_rows, const uint8_t* b,
+                                                  const float* sb, int num_groups, const int32_t* m_indices,
+                                                  int64_t M_tot, int64_t N, int64_t K, int scale_mode,
+                                                  void* stream) {
+  if (M_tot > 0 && N > 0) {
+    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
+    if (v != DG_OK) return v;
+  } else if (out_block_rows != 1 && out_block_rows != 128) {
+    return DG_ERR_INVALID_ARG;
+  }
+  return gemm_grouped(cq, ld_cq, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
+                      a_scale_rows == 1, make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
 }
 
 DG_API int dg_get_device_status(void* stream) {

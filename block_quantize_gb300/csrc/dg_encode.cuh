@@ -1,0 +1,200 @@
+// dg_encode.cuh -- E4M3 encoding shared by the quantizers and the GEMM epilogue
+// that requantizes its FP32 accumulators.
+//
+// The arithmetic is that of the lpnh.cn DeepGEMM walkthrough §4.2 (scale =
+// max|x| / 448, divide, round to the nearest E4M3 value with ties to even) and
+// §5.4 (an all-zero block gets scale 1); power-of-two scales follow the packed
+// UE8M0 scales of pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析" §3.1. The GEMM
+// epilogue variant applies the same steps to the FP32 accumulators before they
+// leave the chip ("quantize on demand at write-back", walkthrough §2.2; fusing
+// the scale computation saves a round trip through memory, §6).
+#pragma once
+
+#include <cuda_fp8.h>
+#include <cstdint>
+
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+
+// Smallest power of two >= s (s > 0, finite), not below 2^-127, the smallest
+// UE8M0 value. Exponent arithmetic on the binary32 encoding.
+__device__ __forceinline__ float pow2_round_up(float s) {
+  const uint32_t b = __float_as_uint(s);
+  const uint32_t e = b >> 23;
+  if (e == 0u) {  // subnormal s < 2^-126
+    return (b <= 0x00400000u) ? __uint_as_float(0x00400000u) : __uint_as_float(0x00800000u);
+  }
+  return __uint_as_float((e + ((b & 0x007FFFFFu) != 0u ? 1u : 0u)) << 23);
+}
+
+// Scale of a block whose largest magnitude is amax: fl32(amax / 448); 1 for an
+// all-zero block (or an underflow to 0); optionally rounded up to a power of two.
+__device__ __forceinline__ float block_scale(float amax, bool pow2) {
+  float s = amax / 448.0f;
+  if (s == 0.0f) s = 1.0f;
+  return pow2 ? pow2_round_up(s) : s;
+}
+
+__device__ __forceinline__ uint32_t cvt2(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// E4M3 codes of fl32(v / s) for the four values of v, packed little-endian.
+// kMode 0: exact division with the r = 1/s fast path (valid for normal s);
+// kMode 1: power-of-two s, v * r exact; kMode 2: plain division (tiny s).
+//
+// Why kMode 0 is exact: q = fl32(v r) with r = fl32(1/s) lies within
+// 1.5 * 2^-23 (relative) of fl32(v / s). If q (1 - 2^-20) and q (1 + 2^-20)
+// round to the same E4M3 code, every value between them -- fl32(v / s)
+// included -- does too (rounding to E4M3 is monotone), so that code is exact.
+// Otherwise (an E4M3 rounding boundary within 2^-20 of q, about one value in
+// 2^15) the element is divided exactly.
+template <int kMode>
+__device__ __forceinline__ uint32_t encode4(const float4 v, float s, float r) {
+  if constexpr (kMode == 2) {
+    return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
+  } else {
+    const float q0 = v.x * r, q1 = v.y * r, q2 = v.z * r, q3 = v.w * r;
+    const uint32_t c = cvt2(q0, q1) | (cvt2(q2, q3) << 16);
+    if constexpr (kMode == 1) {
+      return c;
+    } else {
+      constexpr float kLo = 1.0f - 0x1p-20f, kHi = 1.0f + 0x1p-20f;
+      const uint32_t lo = cvt2(q0 * kLo, q1 * kLo) | (cvt2(q2 * kLo, q3 * kLo) << 16);
+      const uint32_t hi = cvt2(q0 * kHi, q1 * kHi) | (cvt2(q2 * kHi, q3 * kHi) << 16);
+      if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
+      return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
+    }
+  }
+}
+
+template <int kMode>
+__device__ __forceinline__ uint8_t encode1(float v, float s, float r) {
+  const uint32_t c = encode4<kMode>(make_float4(v, 0.f, 0.f, 0.f), s, r);
+  return static_cast<uint8_t>(c & 0xFFu);
+}
+
+// Runtime choice of the encoding mode for scale s.
+__device__ __forceinline__ uint32_t encode4_any(const float4 v, float s, float r, bool pow2) {
+  if (pow2) return encode4<1>(v, s, r);
+  if (s >= 0x1p-126f) return encode4<0>(v, s, r);
+  return encode4<2>(v, s, r);
+}
+
+// ---------------------------------------------------------------------------
+// Requantizing GEMM epilogue.
+//
+// Each epilogue thread holds 64 FP32 accumulators: one output row, 64
+// consecutive columns starting at a multiple of 64. A 128-column output block
+// is covered by two such slices held by warps ew and ew ^ 4 of the same TMEM
+// lane quadrant, and a 128 x 128 block by the eight warps [ew & ~7, +8).
+// The slices' maxima meet in shared memory: every warp writes its values,
+// arrives on the tile parity's exchange barrier (count = number of epilogue
+// warps, release at CTA scope) and waits for it (bounded), then computes the
+// scale, encodes and stores. Two sets of exchange slots alternate between
+// tiles: a warp can only overwrite a set after every warp has arrived on the
+// other set's barrier, i.e. after every read of the set's previous use.
+
+// Shared-memory bytes of the exchange for kEpiWarps epilogue warps (8-byte aligned).
+__host__ __device__ constexpr uint32_t requant_xchg_bytes(int epi_warps) {
+  return 2 * 8 + 2 * epi_warps * 4 + 2 * epi_warps * 32 * 4;
+}
+
+// Initializes the two exchange barriers (one thread, before the CTA's first sync).
+__device__ __forceinline__ void requant_xchg_init(uint8_t* xchg, int epi_warps) {
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xchg);
+  mbar_init(smem_u32(&bar[0]), epi_warps);
+  mbar_init(smem_u32(&bar[1]), epi_warps);
+}
+
+// Requantizes one thread's slice: row `row` (valid: row < M and not a padding
+// row; invalid rows count as zeros and store nothing unless store_zero_row),
+// columns [col0, col0 + 64) of an N-column output, tile sequence number tl
+// (the same for all epilogue warps of the CTA). Returns false if a wait failed
+// (abort raised or timeout); then nothing is stored.
+template <int kEpiWarps>
+__device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], bool row_valid,
+                                                    bool store_zero_row, int row, int M, int N, int col0,
+                                                    int ew, int lane, uint32_t tl, uint8_t* xchg,
+                                                    const RequantOut& o, volatile int* abort,
+                                                    unsigned int* status, uint64_t limit) {
+  uint64_t* bar = reinterpret_cast<uint64_t*>(xchg);
+  const uint32_t p = tl & 1u;
+  float* xw = reinterpret_cast<float*>(xchg + 16) + p * kEpiWarps;
+  float* xv = reinterpret_cast<float*>(xchg + 16 + 2 * kEpiWarps * 4) + p * kEpiWarps * 32;
+
+  float m = 0.f;
+  if (row_valid) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 v = f32x2_split(acc[j]);
+      m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+    }
+  }
+  // Non-negative floats order like their bit patterns.
+  if (o.block_rows == 1) {
+    xv[ew * 32 + lane] = m;
+  } else {
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+    if (lane == 0) xw[ew] = __uint_as_float(wm);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bar[p]));
+  const bool w = mbar_wait(smem_u32(&bar[p]), (tl >> 1) & 1u, abort, status, limit);
+  if (!__all_sync(0xFFFFFFFFu, w)) return false;
+
+  float amax;
+  if (o.block_rows == 1) {
+    amax = fmaxf(m, xv[(ew ^ 4) * 32 + lane]);
+  } else {
+    const int w0 = ew & ~7;
+    amax = xw[w0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, xw[w0 + i]);
+  }
+  const bool pow2 = o.pow2 != 0;
+  const float s = block_scale(amax, pow2);
+  const float r = 1.0f / s;
+  const int sblk = col0 >> 7;  // 128-column block of this slice
+
+  if (col0 < N) {
+    if (o.block_rows == 1) {
+      if ((ew & 4) == 0 && row < M && (row_valid || store_zero_row))
+        o.s[static_cast<int64_t>(row) * o.ld_s + sblk] = s;
+    } else if (ew == (ew & ~7) && lane == 0 && (row & ~127) < M) {
+      // One thread per block; the block's first row is row & ~127.
+      o.s[static_cast<int64_t>(row >> 7) * o.ld_s + sblk] = s;
+    }
+  }
+  if (row >= M || !(row_valid || store_zero_row) || col0 >= N) return true;
+
+  uint8_t* dst = o.q + static_cast<int64_t>(row) * o.ld_q + col0;
+  uint32_t code[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 a = f32x2_split(acc[2 * j]), b = f32x2_split(acc[2 * j + 1]);
+    code[j] = row_valid ? encode4_any(make_float4(a.x, a.y, b.x, b.y), s, r, pow2) : 0u;
+  }
+  if (col0 + 64 <= N) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+  } else {
+    const int n = N - col0;  // 1..63 valid columns
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (4 * j + 3 < n) {
+        *reinterpret_cast<uint32_t*>(dst + 4 * j) = code[j];
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (4 * j + t < n) dst[4 * j + t] = static_cast<uint8_t>(code[j] >> (8 * t));
+      }
+    }
+  }
+  return true;
+}
+
+}  // namespace dg

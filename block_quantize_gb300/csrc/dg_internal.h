@@ -50,6 +50,17 @@ cudaError_t launch_quantize_1x128(const void* x, bool bf16, int64_t rows, int64_
                                   uint8_t* q, int64_t ld_q, float* scales, bool pow2_scales,
                                   cudaStream_t stream);
 
+// E4M3 output of a requantizing GEMM: the FP32 accumulators are encoded with
+// one scale per block of block_rows x 128 output elements.
+struct RequantOut {
+  uint8_t* q;       // [M][ld_q] E4M3 codes (nullptr: bf16 output instead)
+  int64_t ld_q;     // multiple of 16; q 16-byte aligned
+  float* s;         // [M or ceil(M/128)][ld_s] scales
+  int64_t ld_s;     // ceil(N / 128)
+  int block_rows;   // 1 (one scale per row and 128 columns) or 128 (128 x 128 blocks)
+  int pow2;         // scales rounded up to powers of two
+};
+
 // One dense or M-grouped GEMM problem (sizes already validated).
 struct GemmProblem {
   void* c;
@@ -66,10 +77,14 @@ struct GemmProblem {
   int num_sms_cap;           // 0 = every SM
   bool pow2_scales;          // every scale is a power of two (DG_SCALE_UE8M0)
   bool sa_per_row;           // sa is [M][K/128] (one A scale per row and K block)
+  RequantOut rq;             // rq.q != nullptr: E4M3 output instead of bf16 c
 };
 
 // Returns a dg_status value.
 int launch_gemm(const GemmProblem& p, cudaStream_t stream);
+
+// Writes v into n consecutive floats of device memory.
+cudaError_t launch_fill_f32(float* dst, int64_t n, float v, cudaStream_t stream);
 
 // Dense GEMMs with M > 128 on CTA pairs (gemm_pair.cu); DG_ERR_UNSUPPORTED_SHAPE
 // when the problem or the launch limits do not allow a pair kernel.

@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "dg_device.cuh"
+#include "dg_encode.cuh"
 #include "dg_internal.h"
 #include "../../include/dgfp8.h"
 
@@ -61,6 +62,7 @@ constexpr uint32_t kWarpOutBytes = 32 * 32 * 2;  // one warp's 32 x 32 bf16 outp
 
 struct GemmArgs {
   __nv_bfloat16* c;
+  RequantOut rq;   // E4M3 output (requantizing kernels)
   int sa_per_row;  // sa is [M][K/128] instead of [ceil(M/128)][K/128]
   int64_t ld_c;
   const float* sa;
@@ -111,6 +113,14 @@ struct Cfg {
   static_assert(kNumPBuf % kIssuers == 0, "buffer ownership by issuer");
 };
 
+// Shared memory behind the operand ring for the output: bf16 staging boxes, or
+// with requantization (64-column slices only) the slices' maxima exchange.
+template <int BN, bool kQ>
+__host__ __device__ constexpr uint32_t out_bytes() {
+  static_assert(!kQ || Cfg<BN>::kCols == 64, "the requantizing epilogue takes 64-column slices");
+  return kQ ? requant_xchg_bytes(Cfg<BN>::kEpiWarps) : Cfg<BN>::kOutBytes;
+}
+
 // Output tile of persistent iteration t: grouped raster, M fastest inside a
 // group of kGroupM M-blocks.
 __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& mb, int& nb) {
@@ -144,7 +154,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int BN, bool kGrouped>
+template <int BN, bool kGrouped, bool kQ>
 __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
@@ -164,7 +174,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   const size_t a_read_end = static_cast<size_t>(S - 1) * args.a_stage_bytes + kATileBytes;
   if (a_read_end > tail_off) tail_off = a_read_end;
   uint8_t* smem_out = smem + tail_off;  // kEpiWarps boxes of kWarpOutBytes (kTmaStore)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + C::kOutBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + out_bytes<BN, kQ>());
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + kMaxStages;
   uint64_t* tfull_bar = bars + 2 * kMaxStages;
@@ -188,11 +198,12 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       mbar_init(smem_u32(&tempty_bar[b]), C::kEpiWarps);
     }
     mbar_init(smem_u32(drain_bar), C::kIssuers);
+    if constexpr (kQ) requant_xchg_init(smem_out, C::kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if (C::kTmaStore) tma_prefetch_desc(&tmap_c);
+    if (C::kTmaStore && !kQ) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
@@ -296,7 +307,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     bool ready = false;  // the full barrier of K block `it` is known complete
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    uint32_t tl = 0;     // tiles done by this CTA
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tl) {
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       int g = 0;
@@ -395,7 +407,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int row = mb * kBM + row_in_tile;
       bool zero_row = skip;
       if constexpr (kGrouped) zero_row = zero_row || (row < args.M && __ldg(args.m_indices + row) < 0);
-      if constexpr (C::kTmaStore) {
+      if constexpr (kQ) {
+        // Padding rows of the grouped layout are written as zeros (scale 1).
+        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M && !zero_row, kGrouped, row, args.M, args.N, col0,
+                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit)) {
+          ok = false;
+          break;
+        }
+      } else if constexpr (C::kTmaStore) {
         // bf16 row segment -> this warp's 64-byte-swizzled 32 x 32 box (16-byte
         // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA store at
         // (col0 + 32 h, mb*128 + lg*32), clipped at M and N; the two halves
@@ -470,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
       }
     }
-    if (C::kTmaStore && lane == 0 && stores_issued) bulk_wait_all();
+    if (C::kTmaStore && !kQ && lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
   }
 
@@ -493,6 +512,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+}
+
+// dst[i] = v for i < n (grid-stride).
+__global__ void fill_f32_kernel(float* dst, int64_t n, float v) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = v;
 }
 
 // A block whose only wait is on a barrier that nothing arrives at.
@@ -590,11 +616,13 @@ int pick_bn(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-template <int BN, bool kGrouped>
+template <int BN, bool kGrouped, bool kQ>
 int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   using Cf = Cfg<BN>;
+  constexpr uint32_t kOut = out_bytes<BN, kQ>();
   GemmArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
+  args.rq = p.rq;
   args.ld_c = p.ld_c;
   args.sa = p.sa;
   args.sa_per_row = p.sa_per_row ? 1 : 0;
@@ -614,7 +642,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
   const uint32_t stage_bytes = args.a_stage_bytes + Cf::kBTileBytes;
   const size_t bar_bytes = (2 * kMaxStages + 2 * Cf::kNumPBuf + 1) * sizeof(uint64_t) + 16;
-  const size_t budget = kMaxDynSmem - 1024 - Cf::kOutBytes - bar_bytes;
+  const size_t budget = kMaxDynSmem - 1024 - kOut - bar_bytes;
   // The operand ring, including the padding a short A box needs (see the kernel).
   auto ring_bytes = [&](int st) {
     return std::max<size_t>(static_cast<size_t>(st) * stage_bytes,
@@ -628,7 +656,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   stages = stages / Cf::kIssuers * Cf::kIssuers;
   if (stages < Cf::kIssuers || ring_bytes(stages) > budget) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_stages = stages;
-  size_t smem = 1024 + ring_bytes(stages) + Cf::kOutBytes + bar_bytes;
+  size_t smem = 1024 + ring_bytes(stages) + kOut + bar_bytes;
   // One CTA per SM: the grid is persistent and each CTA owns its SM's TMEM.
   smem = std::max<size_t>(smem, kMinSmemPerCta);
   if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
@@ -653,7 +681,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
     const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
     if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
   }
-  if (Cf::kTmaStore) {
+  if (Cf::kTmaStore && !kQ) {
     // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_c) * 2};
@@ -662,10 +690,10 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
                     CU_TENSOR_MAP_SWIZZLE_64B))
       return DG_ERR_CUDA;
   } else {
-    tc = ta;  // not read by narrow tiles
+    tc = ta;  // not read by narrow tiles or the requantizing epilogue
   }
 
-  auto kernel = fp8_gemm_kernel<BN, kGrouped>;
+  auto kernel = fp8_gemm_kernel<BN, kGrouped, kQ>;
   static std::atomic<uint64_t> attr_set{0};
   if (dev < 64 && !(attr_set.load() & (1ull << dev))) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -733,19 +761,31 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
   const int sms = device_info(dev).num_sms;
   if (sms <= 0) return DG_ERR_NO_DEVICE;
-  if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
+  // Decode shapes (M <= 128) with bf16 output: cluster split-K. The
+  // requantizing epilogue needs a tile's full rows, so it takes the kernels below.
+  if (!block_n_override() && p.rq.q == nullptr && small_m_supported(p.M, p.m_indices))
+    return launch_gemm_small_m(p, stream);
   if (!block_n_override() && p.m_indices == nullptr && p.M > kBM) {
     const int r = launch_gemm_pair(p, stream);
     if (r != DG_ERR_UNSUPPORTED_SHAPE) return r;
   }
-  const int bn = pick_bn(p.M, p.N, sms);
   const bool grouped = p.m_indices != nullptr;
+  if (p.rq.q != nullptr) {
+    // The requantizing epilogue needs whole 128-column output blocks per tile.
+    const int bn = (block_n_override() == 128 || (!block_n_override() && p.M <= 2 * kBM)) ? 128 : 256;
+    if (bn == 128)
+      return grouped ? run_gemm<128, true, true>(p, stream, dev, sms) : run_gemm<128, false, true>(p, stream, dev, sms);
+    return grouped ? run_gemm<256, true, true>(p, stream, dev, sms) : run_gemm<256, false, true>(p, stream, dev, sms);
+  }
+  const int bn = pick_bn(p.M, p.N, sms);
   switch (bn) {
-    case 16: return grouped ? run_gemm<16, true>(p, stream, dev, sms) : run_gemm<16, false>(p, stream, dev, sms);
-    case 32: return grouped ? run_gemm<32, true>(p, stream, dev, sms) : run_gemm<32, false>(p, stream, dev, sms);
-    case 64: return grouped ? run_gemm<64, true>(p, stream, dev, sms) : run_gemm<64, false>(p, stream, dev, sms);
-    case 128: return grouped ? run_gemm<128, true>(p, stream, dev, sms) : run_gemm<128, false>(p, stream, dev, sms);
-    default: return grouped ? run_gemm<256, true>(p, stream, dev, sms) : run_gemm<256, false>(p, stream, dev, sms);
+    case 16: return grouped ? run_gemm<16, true, false>(p, stream, dev, sms) : run_gemm<16, false, false>(p, stream, dev, sms);
+    case 32: return grouped ? run_gemm<32, true, false>(p, stream, dev, sms) : run_gemm<32, false, false>(p, stream, dev, sms);
+    case 64: return grouped ? run_gemm<64, true, false>(p, stream, dev, sms) : run_gemm<64, false, false>(p, stream, dev, sms);
+    case 128:
+      return grouped ? run_gemm<128, true, false>(p, stream, dev, sms) : run_gemm<128, false, false>(p, stream, dev, sms);
+    default:
+      return grouped ? run_gemm<256, true, false>(p, stream, dev, sms) : run_gemm<256, false, false>(p, stream, dev, sms);
   }
 }
 
@@ -754,6 +794,13 @@ cudaError_t read_and_clear_status(unsigned int* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_status_word, sizeof(unsigned int));
   if (e != cudaSuccess) return e;
   return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(unsigned int));
+}
+
+cudaError_t launch_fill_f32(float* dst, int64_t n, float v, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  fill_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dst, n, v);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {

@@ -43,6 +43,7 @@
 
 #include "../../include/dgfp8.h"
 #include "dg_device.cuh"
+#include "dg_encode.cuh"
 #include "dg_internal.h"
 
 namespace dg {
@@ -62,20 +63,25 @@ constexpr uint32_t kBoxBytes = 32 * 32 * 2;        // one warp's 32 x 32 bf16 ou
 constexpr size_t kMaxDynSmem = 227 * 1024;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(2 * kBM, kBN);
 
-template <int kEpiCols>
+template <int kEpiCols, bool kQ>
 struct PCfg {
   static constexpr int kEpiPerQuad = kBN / kEpiCols;  // warps per TMEM lane quadrant
   static constexpr int kEpiWarps = 4 * kEpiPerQuad;
   static constexpr int kFirstEpiWarp = 1 + kIssuers;
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
-  static constexpr uint32_t kOutBytes = kEpiWarps * kBoxBytes * (kEpiCols / 32);
+  // bf16 output: staging boxes for the TMA stores; E4M3 output: the slices'
+  // maxima exchange (codes are stored straight from registers).
+  static constexpr uint32_t kOutBytes =
+      kQ ? requant_xchg_bytes(kEpiWarps) : kEpiWarps * kBoxBytes * (kEpiCols / 32);
+  static_assert(!kQ || kEpiCols == 64, "the requantizing epilogue takes 64-column slices");
   static_assert(kEpiCols == 32 || kEpiCols == 64, "epilogue slice");
   static_assert(kThreads <= 1024, "CTA size");
 };
 constexpr int kEpiCols = 64;
 
 struct PairArgs {
-  __nv_bfloat16* c;
+  __nv_bfloat16* c;  // bf16 output (kernels without requantization)
+  RequantOut rq;     // E4M3 output and scales (requantizing kernels)
   int64_t ld_c;
   int sa_per_row;  // sa is [M][K/128] instead of [ceil(M/128)][K/128]
   const float* sa;
@@ -201,12 +207,12 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
   }
 }
 
-template <int EC>
-__global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
+template <int EC, bool kQ>
+__global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_c, const PairArgs args) {
-  using C = PCfg<EC>;
+  using C = PCfg<EC, kQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -241,11 +247,12 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
       mbar_init(smem_u32(&tempty_bar[b]), 2 * C::kEpiWarps);
     }
     mbar_init(smem_u32(drain_bar), kIssuers);
+    if constexpr (kQ) requant_xchg_init(smem_out, C::kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    tma_prefetch_desc(&tmap_c);
+    if constexpr (!kQ) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kNumBuf * kBN);
   tc_fence_before();
@@ -312,9 +319,10 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
     uint8_t* out_box = smem_out + ew * kBoxBytes * (EC / 32);
     bool stores_issued = false;
     uint32_t it = 0;
+    uint32_t tl = 0;  // tiles done by this pair
     bool ok = true;
     bool ready = false;  // the full barrier of slot `it` is known to be complete
-    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
+    for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
       int pm, nb;
       pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
@@ -357,7 +365,16 @@ __global__ void __launch_bounds__(PCfg<EC>::kThreads, 1)
       if (!ok) break;
 
       const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
-      store_tile_rows<EC>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane, stores_issued);
+      if constexpr (kQ) {
+        const int row = row0 + lane;
+        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, row, args.M, args.N, nb * kBN + part * EC,
+                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit)) {
+          ok = false;
+          break;
+        }
+      } else {
+        store_tile_rows<EC>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane, stores_issued);
+      }
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
@@ -435,7 +452,9 @@ constexpr uint32_t kIdescScaled = idesc_e4m3_block_scaled(2 * kBM, kBN);
 constexpr int kNatEpiWarps = 8;                        // 4 quadrants x 2 slices of 64 columns
 constexpr int kNatFirstEpiWarp = 8;
 constexpr int kNatThreads = 32 * (kNatFirstEpiWarp + kNatEpiWarps);
-constexpr uint32_t kNatOutBytes = kNatEpiWarps * kBoxBytes * 2;
+__host__ __device__ constexpr uint32_t nat_out_bytes(bool requant) {
+  return requant ? requant_xchg_bytes(kNatEpiWarps) : kNatEpiWarps * kBoxBytes * 2;
+}
 static_assert(kAccCols + kNatMaxStages * kNatKbPerStage * kSfCols <= 512, "TMEM");
 
 // Biased exponent of a power-of-two FP32 scale = its UE8M0 code (2^-127,
@@ -444,6 +463,7 @@ __device__ __forceinline__ uint32_t ue8m0_word(float s) {
   return 0x01010101u * ((__float_as_uint(s) >> 23) & 0xFFu);
 }
 
+template <bool kQ>
 __global__ void __launch_bounds__(kNatThreads, 1)
     fp8_gemm_pair_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
@@ -454,7 +474,7 @@ __global__ void __launch_bounds__(kNatThreads, 1)
   const int S = args.num_stages;
   uint8_t* ring = smem;
   uint8_t* smem_out = smem + static_cast<size_t>(S) * kNatStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + kNatOutBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + nat_out_bytes(kQ));
   uint64_t* full_bar = bars;                       // even CTA: operands and scales of both CTAs
   uint64_t* empty_bar = bars + kNatMaxStages;      // the stage's MMAs are done
   uint64_t* tfull_bar = bars + 2 * kNatMaxStages;  // [2] the tile's accumulator is final
@@ -484,12 +504,13 @@ __global__ void __launch_bounds__(kNatThreads, 1)
       mbar_init(smem_u32(&tempty_bar[b]), 2 * kNatEpiWarps);
     }
     mbar_init(smem_u32(drain_bar), 2);
+    if constexpr (kQ) requant_xchg_init(smem_out, kNatEpiWarps);
     *abort_flag = 0;
     *issue_turn = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    tma_prefetch_desc(&tmap_c);
+    if constexpr (!kQ) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), 512);
   tc_fence_before();
@@ -659,7 +680,14 @@ __global__ void __launch_bounds__(kNatThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] = f32x2(r[2 * j], r[2 * j + 1]);
       const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
-      store_tile_rows<64>(acc, tmap_c, args, out_box, row0, nb * kBN + part * 64, lane, stores_issued);
+      if constexpr (kQ) {
+        const int row = row0 + lane;
+        if (!requant_store_slice<kNatEpiWarps>(acc, row < args.M, false, row, args.M, args.N, nb * kBN + part * 64,
+                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit))
+          break;
+      } else {
+        store_tile_rows<64>(acc, tmap_c, args, out_box, row0, nb * kBN + part * 64, lane, stores_issued);
+      }
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
@@ -708,26 +736,32 @@ struct PairKind {
   int max_stages;
   int kb_per_stage;
 };
-PairKind pair_kind(bool scaled) {
+template <bool kQ>
+PairKind pair_kind_t(bool scaled) {
+  using C = PCfg<kEpiCols, kQ>;
   if (scaled)
-    return {fp8_gemm_pair_scaled_kernel, kNatThreads,
-            kNatOutBytes + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, kNatStageBytes, kNatMaxStages,
+    return {fp8_gemm_pair_scaled_kernel<kQ>, kNatThreads,
+            nat_out_bytes(kQ) + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, kNatStageBytes, kNatMaxStages,
             kNatKbPerStage};
-  return {fp8_gemm_pair_kernel<kEpiCols>, PCfg<kEpiCols>::kThreads,
-          PCfg<kEpiCols>::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes,
-          kMaxStages, 1};
+  return {fp8_gemm_pair_kernel<kEpiCols, kQ>, C::kThreads,
+          C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
+}
+// variant = scaled + 2 * requant
+PairKind pair_kind(int variant) {
+  const bool scaled = (variant & 1) != 0;
+  return (variant & 2) ? pair_kind_t<true>(scaled) : pair_kind_t<false>(scaled);
 }
 
 // Largest number of co-resident CTA pairs of a kernel (cached per device).
-int max_active_pairs(bool scaled, size_t smem) {
+int max_active_pairs(int variant, size_t smem) {
   static std::mutex mu;
-  static int cache[64][2] = {};
+  static int cache[64][4] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][scaled ? 1 : 0];
+  int& c = cache[dev][variant];
   if (c == 0) {
-    const PairKind k = pair_kind(scaled);
+    const PairKind k = pair_kind(variant);
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -749,13 +783,13 @@ int max_active_pairs(bool scaled, size_t smem) {
   return c;
 }
 
-bool set_pair_smem_attribute(bool scaled) {
-  static std::atomic<uint64_t> done[2] = {{0}, {0}};
+bool set_pair_smem_attribute(int variant) {
+  static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  std::atomic<uint64_t>& d = done[scaled ? 1 : 0];
+  std::atomic<uint64_t>& d = done[variant];
   if (d.load() & (1ull << dev)) return true;
-  if (cudaFuncSetAttribute(pair_kind(scaled).kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(pair_kind(variant).kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kMaxDynSmem)) != cudaSuccess)
     return false;
   d.fetch_or(1ull << dev);
@@ -771,10 +805,13 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   // The block-scaled kernel fills its scale columns uniformly, which needs one
   // A scale per 128 rows; per-row A scales take the FP32 promotion (exact too).
   const bool scaled = p.pow2_scales && !p.sa_per_row;
-  const PairKind kind = pair_kind(scaled);
+  const bool requant = p.rq.q != nullptr;
+  const int variant = (scaled ? 1 : 0) + (requant ? 2 : 0);
+  const PairKind kind = pair_kind(variant);
   PairArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
+  args.rq = p.rq;
   args.sa = p.sa;
   args.sa_per_row = p.sa_per_row ? 1 : 0;
   args.sb = p.sb;
@@ -793,10 +830,10 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   if (stages < 4) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_stages = stages;
   const size_t smem = 1024 + static_cast<size_t>(stages) * kind.stage_bytes + kind.fixed_smem;
-  if (!set_pair_smem_attribute(scaled)) return DG_ERR_CUDA;
+  if (!set_pair_smem_attribute(variant)) return DG_ERR_CUDA;
 
   const int64_t tiles = static_cast<int64_t>(args.num_pm) * args.num_nb;
-  int pairs = max_active_pairs(scaled, smem);
+  int pairs = max_active_pairs(variant, smem);
   if (pairs <= 0) return DG_ERR_UNSUPPORTED_SHAPE;
   if (p.num_sms_cap > 0) pairs = std::min(pairs, p.num_sms_cap / 2);
   pairs = static_cast<int>(std::min<int64_t>(pairs, tiles));
@@ -826,7 +863,9 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
         !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true))
       return DG_ERR_CUDA;
   }
-  {
+  if (requant) {
+    tc = ta;  // not read: the requantizing epilogue stores from registers
+  } else {
     // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_c) * 2};

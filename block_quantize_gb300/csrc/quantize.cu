@@ -49,6 +49,7 @@
 #include <cstdint>
 
 #include "dg_device.cuh"
+#include "dg_encode.cuh"
 #include "dg_internal.h"
 
 namespace dg {
@@ -58,49 +59,6 @@ constexpr int kBlock = 128;
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = kBlock / kWarps;  // 8
-
-// Smallest power of two >= s (s > 0, finite), not below 2^-127, the smallest
-// UE8M0 value. Exponent arithmetic on the binary32 encoding.
-__device__ __forceinline__ float pow2_round_up(float s) {
-  const uint32_t b = __float_as_uint(s);
-  const uint32_t e = b >> 23;
-  if (e == 0u) {  // subnormal s < 2^-126
-    return (b <= 0x00400000u) ? __uint_as_float(0x00400000u) : __uint_as_float(0x00800000u);
-  }
-  return __uint_as_float((e + ((b & 0x007FFFFFu) != 0u ? 1u : 0u)) << 23);
-}
-
-__device__ __forceinline__ uint32_t cvt2(float a, float b) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-
-// E4M3 codes of fl32(v / s) for the four values of v, packed little-endian.
-// kMode 0: exact division with the r = 1/s fast path (valid for normal s);
-// kMode 1: power-of-two s, v * r exact; kMode 2: plain division (tiny s).
-template <int kMode>
-__device__ __forceinline__ uint32_t encode4(const float4 v, float s, float r) {
-  if constexpr (kMode == 2) {
-    return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
-  } else {
-    const float q0 = v.x * r, q1 = v.y * r, q2 = v.z * r, q3 = v.w * r;
-    const uint32_t c = cvt2(q0, q1) | (cvt2(q2, q3) << 16);
-    if constexpr (kMode == 1) {
-      return c;
-    } else {
-      constexpr float kLo = 1.0f - 0x1p-20f, kHi = 1.0f + 0x1p-20f;
-      const uint32_t lo = cvt2(q0 * kLo, q1 * kLo) | (cvt2(q2 * kLo, q3 * kLo) << 16);
-      const uint32_t hi = cvt2(q0 * kHi, q1 * kHi) | (cvt2(q2 * kHi, q3 * kHi) << 16);
-      if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
-      return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
-    }
-  }
-}
-
-template <int kMode>
-__device__ __forceinline__ uint8_t encode1(float v, float s, float r) {
-  const uint32_t c = encode4<kMode>(make_float4(v, 0.f, 0.f, 0.f), s, r);
-  return static_cast<uint8_t>(c & 0xFFu);
-}
 
 template <int kMode, bool kVec>
 __device__ __forceinline__ void encode_store(const float4 (&v)[kRowsPerWarp], int64_t r0, int64_t c0,

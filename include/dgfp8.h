@@ -13,7 +13,11 @@
  *      §4.1 fp8_gemm_nt(c, a, b, a_sf, b_sf));
  *   3. the M-grouped contiguous variant for MoE experts, where each 128-row
  *      block of A belongs to one expert whose B and scales it uses (pzsr.cn
- *      page §2.3, §3.2, §3.3).
+ *      page §2.3, §3.2, §3.3);
+ *   4. both GEMMs with their FP32 accumulators requantized to E4M3 codes plus
+ *      block scales in the epilogue instead of rounded to bf16 (walkthrough
+ *      §2.2: quantize on demand at write-back; §6: fuse the scale computation
+ *      into the kernel to save a round trip through memory).
  *
  * Conventions shared by every entry point:
  *   - Every data pointer is a DEVICE pointer that the caller allocated and owns;
@@ -46,7 +50,7 @@ extern "C" {
 #define DG_API __attribute__((visibility("default")))
 #endif
 
-#define DG_ABI_VERSION 2u
+#define DG_ABI_VERSION 3u
 
 typedef enum {
     DG_OK = 0,
@@ -175,6 +179,45 @@ DG_API int dg_fp8_grouped_gemm_contiguous_1x128(void *c, int64_t ld_c,
                                                 const int32_t *m_indices,
                                                 int64_t M_tot, int64_t N, int64_t K,
                                                 int scale_mode, void *stream);
+
+/* Dense NT GEMM with the output requantized in the epilogue (walkthrough §2.2
+ * "quantize on demand at write-back", §6 fusing the scale computation): the
+ * FP32 accumulator value v[m, n] of dg_fp8_gemm_nt (before any bf16 rounding)
+ * is quantized by the steps of dg_quantize_fp8_block with blocks of
+ * out_block_rows x 128 elements of C:
+ *   cq  [M][ld_cq] E4M3 codes out: RNE of fl32(v / s), saturated to +-448
+ *   cs  scales out, FP32, s = fl32(max|v| / 448) over the block (1.0 for an
+ *       all-zero block; rounded up to a power of two with out_scale_mode =
+ *       DG_SCALE_UE8M0):
+ *         out_block_rows = 1:   [M][ceil(N/128)]  (per-row activation scales,
+ *                               the sa layout of dg_fp8_gemm_nt_1x128)
+ *         out_block_rows = 128: [ceil(M/128)][ceil(N/128)]
+ *   a_scale_rows  128: sa is [ceil(M/128)][K/128] (dg_fp8_gemm_nt);
+ *                 1:   sa is [M][K/128] (dg_fp8_gemm_nt_1x128)
+ * The operands, scale_mode and their rules are those of dg_fp8_gemm_nt. cq
+ * must be 16-byte aligned with ld_cq >= N a multiple of 16; cs 4-byte aligned.
+ * Bad out_block_rows, a_scale_rows or out_scale_mode give DG_ERR_INVALID_ARG.
+ * M == 0 or N == 0 is a no-op; K == 0 writes codes 0 and scales 1. */
+DG_API int dg_fp8_gemm_nt_requant(uint8_t *cq, int64_t ld_cq, float *cs, int out_block_rows,
+                                  int out_scale_mode,
+                                  const uint8_t *a, int64_t ld_a, const float *sa, int a_scale_rows,
+                                  const uint8_t *b, int64_t ld_b, const float *sb,
+                                  int64_t M, int64_t N, int64_t K,
+                                  int scale_mode, void *stream);
+
+/* M-grouped contiguous GEMM with the output requantized as in
+ * dg_fp8_gemm_nt_requant. Padding rows (m_indices -1) get codes 0 and, with
+ * out_block_rows = 1, scale 1; they count as zeros in a 128 x 128 block.
+ * sa is [M_tot / a_scale_rows][K/128]; the other arguments and rules are those
+ * of dg_fp8_grouped_gemm_contiguous. */
+DG_API int dg_fp8_grouped_gemm_contiguous_requant(uint8_t *cq, int64_t ld_cq, float *cs,
+                                                  int out_block_rows, int out_scale_mode,
+                                                  const uint8_t *a, int64_t ld_a, const float *sa,
+                                                  int a_scale_rows,
+                                                  const uint8_t *b, const float *sb, int num_groups,
+                                                  const int32_t *m_indices,
+                                                  int64_t M_tot, int64_t N, int64_t K,
+                                                  int scale_mode, void *stream);
 
 /* Synchronize `stream`, then read and clear the current device's status word.
  * Returns DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last

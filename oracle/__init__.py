@@ -12,6 +12,9 @@ numpy arrays. Every function cites the page section it follows:
   max|x| / 448 in FP32, divide, round to nearest-even E4M3; §5.4 all-zero block.
 * pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析", §3.1: NT layout, FP32 or
   power-of-two (UE8M0) scales; §2.3/§3.2: M-grouped GEMM for MoE experts.
+* lpnh.cn walkthrough §2.2 (accumulate in FP32, quantize on demand at
+  write-back) and §6 (fuse the scale computation into the kernel): the
+  requantized GEMM output, ``requantize_output`` / ``gemm_nt_requant``.
 """
 from __future__ import annotations
 
@@ -222,3 +225,48 @@ def dequantize(q, s) -> np.ndarray:
     rows, cols = q.shape
     expand = np.repeat(np.repeat(np.asarray(s, dtype=np.float64), BLOCK, axis=0), BLOCK, axis=1)
     return vals * expand[:rows, :cols]
+
+
+def dequantize_1x128(q, s) -> np.ndarray:
+    """float64 values dec(q) * s with one scale per row and 128 columns (a test helper)."""
+    t = e4m3_table()
+    q = np.asarray(q, dtype=np.uint8)
+    expand = np.repeat(np.asarray(s, dtype=np.float64), BLOCK, axis=1)
+    return t[q] * expand[:, :q.shape[1]]
+
+
+def requantize_output(c, out_block_rows: int = 1, mode: int = SCALE_FP32):
+    """The GEMM result requantized at write-back (walkthrough §2.2: the product
+    is accumulated in FP32 and quantized on demand when written back; §6: the
+    scale computation fused into the kernel). The value quantized is the FP32
+    accumulator: the float64 result c rounded once to FP32. The steps are those
+    of §4.2 with blocks of out_block_rows x 128 (1: per-row activation scales,
+    pzsr.cn page §3.1; 128: the 128 x 128 blocks of §4.2).
+
+    Returns (q uint8, scales float32 [rows or ceil(rows/128), ceil(cols/128)]).
+    """
+    v = np.asarray(c, dtype=np.float64).astype(np.float32)
+    if out_block_rows == 1:
+        return quantize_1x128(v, mode)
+    if out_block_rows == BLOCK:
+        return quantize(v, mode)
+    raise ValueError("out_block_rows must be 1 or 128")
+
+
+def gemm_nt_requant(qa, sa, qb, sb, out_block_rows: int = 1, mode: int = SCALE_FP32, rows=None,
+                    a_1x128: bool = False):
+    """gemm_nt followed by requantize_output on the selected rows (for
+    out_block_rows = 128 the rows must be whole 128-row blocks in order, a
+    short last block only at the end). Returns (q, scales, C, E)."""
+    c, e = gemm_nt(qa, sa, qb, sb, rows=rows, a_1x128=a_1x128)
+    q, s = requantize_output(c, out_block_rows, mode)
+    return q, s, c, e
+
+
+def grouped_gemm_requant(qa, sa, qb, sb, m_indices, out_block_rows: int = 1, mode: int = SCALE_FP32,
+                         rows=None, a_1x128: bool = False):
+    """grouped_gemm_contiguous followed by requantize_output (padding rows are
+    zeros, so their codes are 0). Returns (q, scales, C, E)."""
+    c, e = grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=rows, a_1x128=a_1x128)
+    q, s = requantize_output(c, out_block_rows, mode)
+    return q, s, c, e

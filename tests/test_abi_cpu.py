@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_strings_alignment(L):
-    assert bq.dg_get_abi_version() == 2
+    assert bq.dg_get_abi_version() == 3
     assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
     for s in range(7):
         assert bq.dg_status_string(s)
@@ -74,6 +74,24 @@ def grouped_rows(L, **kw):
     return L.dg_fp8_grouped_gemm_contiguous_1x128(a["c"], a["ldc"], a["a"], a["lda"], a["sa"], a["b"],
                                                   a["sb"], a["g"], a["mi"], a["m"], a["n"], a["k"],
                                                   a["mode"], None)
+
+
+def gemm_rq(L, **kw):
+    a = dict(q=P, ldq=256, s=P, br=1, omode=0, a=P, lda=512, sa=P, arows=128, b=P, ldb=512, sb=P,
+             m=128, n=256, k=512, mode=0)
+    a.update(kw)
+    return L.dg_fp8_gemm_nt_requant(a["q"], a["ldq"], a["s"], a["br"], a["omode"], a["a"], a["lda"], a["sa"],
+                                    a["arows"], a["b"], a["ldb"], a["sb"], a["m"], a["n"], a["k"], a["mode"],
+                                    None)
+
+
+def grouped_rq(L, **kw):
+    a = dict(q=P, ldq=256, s=P, br=1, omode=0, a=P, lda=512, sa=P, arows=128, b=P, sb=P, g=2, mi=P,
+             m=256, n=256, k=512, mode=0)
+    a.update(kw)
+    return L.dg_fp8_grouped_gemm_contiguous_requant(a["q"], a["ldq"], a["s"], a["br"], a["omode"], a["a"],
+                                                    a["lda"], a["sa"], a["arows"], a["b"], a["sb"], a["g"],
+                                                    a["mi"], a["m"], a["n"], a["k"], a["mode"], None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -139,6 +157,28 @@ def test_rowwise_grouped_argument_errors(L, kw, status):
     assert grouped_rows(L, **kw) == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=NULL), bq.DG_ERR_INVALID_ARG), (dict(s=NULL), bq.DG_ERR_INVALID_ARG),
+    (dict(br=64), bq.DG_ERR_INVALID_ARG), (dict(br=0), bq.DG_ERR_INVALID_ARG),
+    (dict(omode=2), bq.DG_ERR_INVALID_ARG), (dict(arows=2), bq.DG_ERR_INVALID_ARG),
+    (dict(ldq=192), bq.DG_ERR_INVALID_ARG), (dict(mode=3), bq.DG_ERR_INVALID_ARG),
+    (dict(ldq=264), bq.DG_ERR_MISALIGNED), (dict(q=P + 8), bq.DG_ERR_MISALIGNED),
+    (dict(s=P + 2), bq.DG_ERR_MISALIGNED), (dict(k=500), bq.DG_ERR_UNSUPPORTED_SHAPE),
+    (dict(m=0), bq.DG_OK), (dict(n=0, q=NULL, s=NULL), bq.DG_OK), (dict(m=0, br=3), bq.DG_ERR_INVALID_ARG),
+])
+def test_requant_gemm_argument_errors(L, kw, status):
+    assert gemm_rq(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(mi=NULL), bq.DG_ERR_INVALID_ARG), (dict(br=2), bq.DG_ERR_INVALID_ARG),
+    (dict(m=200), bq.DG_ERR_UNSUPPORTED_SHAPE), (dict(ldq=64), bq.DG_ERR_INVALID_ARG),
+    (dict(ldq=264), bq.DG_ERR_MISALIGNED), (dict(m=0), bq.DG_OK),
+])
+def test_requant_grouped_argument_errors(L, kw, status):
+    assert grouped_rq(L, **kw) == status
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_arguments_without_gpu_report_no_device(L):
     assert gemm(L) == bq.DG_ERR_NO_DEVICE
@@ -148,6 +188,9 @@ def test_valid_arguments_without_gpu_report_no_device(L):
     assert quant_rows(L, dtype=1) == bq.DG_ERR_NO_DEVICE
     assert gemm_rows(L) == bq.DG_ERR_NO_DEVICE
     assert grouped_rows(L) == bq.DG_ERR_NO_DEVICE
+    assert gemm_rq(L) == bq.DG_ERR_NO_DEVICE
+    assert gemm_rq(L, br=128, omode=1, arows=1) == bq.DG_ERR_NO_DEVICE
+    assert grouped_rq(L) == bq.DG_ERR_NO_DEVICE
     assert L.dg_selftest_wait_timeout(1000, None) == bq.DG_ERR_NO_DEVICE
 
 
