@@ -14,6 +14,9 @@ The three compute calls carry the C names:
   pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析" §4.1.
 * ``dg_fp8_grouped_gemm_contiguous(c, a, b, sa, sb, m_indices, scale_mode)``:
   the M-grouped contiguous MoE variant (same page §2.3, §3.2).
+* ``dg_fp8_gemm(c, a, b, sa, sb, layout, scale_mode)``: the dense GEMM in any of
+  the layouts NT, TN, NN, TT; ``dg_fp8_k_grouped_gemm_tn(c, a, b, sa, sb,
+  k_sizes, scale_mode)``: the K-grouped GEMM (same page §3.1, §3.2).
 * ``dg_fp8_gemm_nt_requant`` / ``dg_fp8_grouped_gemm_contiguous_requant``: the
   same GEMMs with the FP32 accumulators requantized to E4M3 codes plus block
   scales in the epilogue (walkthrough §2.2, §6); they return ``(cq, cs)``.
@@ -34,7 +37,8 @@ __all__ = [
     "dg_set_num_sms", "dg_get_num_sms", "dg_quantize_fp8_block", "dg_fp8_gemm_nt",
     "dg_fp8_grouped_gemm_contiguous", "dg_get_device_status", "dg_selftest_wait_timeout",
     "dg_quantize_fp8_1x128", "dg_fp8_gemm_nt_1x128", "dg_fp8_grouped_gemm_contiguous_1x128",
-    "dg_fp8_gemm_nt_requant", "dg_fp8_grouped_gemm_contiguous_requant",
+    "dg_fp8_gemm_nt_requant", "dg_fp8_grouped_gemm_contiguous_requant", "dg_fp8_gemm",
+    "dg_fp8_k_grouped_gemm_tn", "DG_LAYOUT_NT", "DG_LAYOUT_TN", "DG_LAYOUT_NN", "DG_LAYOUT_TT",
     "declared_functions",
 ]
 
@@ -53,6 +57,11 @@ DG_SCALE_FP32 = 0
 DG_SCALE_UE8M0 = 1
 DG_INPUT_FP32 = 0
 DG_INPUT_BF16 = 1
+DG_LAYOUT_NT = 0
+DG_LAYOUT_TN = 1
+DG_LAYOUT_NN = 2
+DG_LAYOUT_TT = 3
+_LAYOUTS = {"NT": DG_LAYOUT_NT, "TN": DG_LAYOUT_TN, "NN": DG_LAYOUT_NN, "TT": DG_LAYOUT_TT}
 BLOCK = 128
 
 _lock = threading.Lock()
@@ -106,6 +115,10 @@ def lib() -> ctypes.CDLL:
         L.dg_fp8_grouped_gemm_contiguous_requant.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, i32, vp, vp,
                                                              i32, vp, i64, i64, i64, i32, vp]
         L.dg_fp8_grouped_gemm_contiguous_requant.restype = i32
+        L.dg_fp8_gemm.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, i64, i64, i32, i32, vp]
+        L.dg_fp8_gemm.restype = i32
+        L.dg_fp8_k_grouped_gemm_tn.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i32, vp, i64, i64, i32, vp]
+        L.dg_fp8_k_grouped_gemm_tn.restype = i32
         L.dg_get_device_status.argtypes = [vp]
         L.dg_get_device_status.restype = i32
         L.dg_selftest_wait_timeout.argtypes = [i64, vp]
@@ -300,6 +313,75 @@ def _grouped(c, a, b, sa, sb, m_indices, scale_mode, a_1x128):
         ctypes.c_void_p(sb.data_ptr()), g, ctypes.c_void_p(m_indices.data_ptr()),
         m_tot, n, k, int(scale_mode), _stream(c))
     _check(st, "dg_fp8_grouped_gemm_contiguous_1x128" if a_1x128 else "dg_fp8_grouped_gemm_contiguous")
+    return c
+
+
+def dg_fp8_gemm(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor,
+                layout="NT", scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
+    """c[M, N] (bf16) = op(A) . op(B) with per-block scales in layout NT, TN,
+    NN or TT (a dg_layout value or its name): a is [M, K] for N-A and [K, M]
+    for T-A; b is [N, K] for T-B and [K, N] for N-B. sa [ceil(M/128), K/128],
+    sb [ceil(N/128), K/128] whatever the layout. Returns c."""
+    lay = _LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    if lay not in _LAYOUTS.values():
+        raise ValueError(f"unknown layout {layout}")
+    a_t = lay in (DG_LAYOUT_TN, DG_LAYOUT_TT)
+    b_n = lay in (DG_LAYOUT_TN, DG_LAYOUT_NN)
+    a, b = _u8(a), _u8(b)
+    _cuda(c, torch.bfloat16, "c")
+    _cuda(a, torch.uint8, "a")
+    _cuda(b, torch.uint8, "b")
+    _cuda(sa, torch.float32, "sa")
+    _cuda(sb, torch.float32, "sb")
+    m, n = c.shape
+    k = a.shape[0] if a_t else a.shape[1]
+    if (a.shape[1] if a_t else a.shape[0]) != m:
+        raise ValueError("a does not match c's M")
+    if tuple(b.shape) != ((k, n) if b_n else (n, k)):
+        raise ValueError("b does not match the layout, K or c's N")
+    kb = k // BLOCK
+    if tuple(sa.shape) != ((m + BLOCK - 1) // BLOCK, kb) or tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
+        raise ValueError("scale shape mismatch")
+    if not (sa.is_contiguous() and sb.is_contiguous()):
+        raise ValueError("scales must be contiguous")
+    st = lib().dg_fp8_gemm(ctypes.c_void_p(c.data_ptr()), _ld(c, "c", 8), ctypes.c_void_p(a.data_ptr()),
+                           _ld(a, "a"), ctypes.c_void_p(sa.data_ptr()), ctypes.c_void_p(b.data_ptr()),
+                           _ld(b, "b"), ctypes.c_void_p(sb.data_ptr()), m, n, k, lay, int(scale_mode),
+                           _stream(c))
+    _check(st, "dg_fp8_gemm")
+    return c
+
+
+def dg_fp8_k_grouped_gemm_tn(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor,
+                             sb: torch.Tensor, k_sizes, scale_mode: int = DG_SCALE_FP32) -> torch.Tensor:
+    """K-grouped TN GEMM: c[g] (bf16 [M, N]) = A[k range g]^T . B[k range g]
+    for a [K_tot, M], b [K_tot, N], sa [ceil(M/128), K_tot/128],
+    sb [ceil(N/128), K_tot/128] and host group sizes k_sizes (multiples of
+    128). c is [G, M, N] with contiguous groups. Returns c."""
+    sizes = [int(v) for v in k_sizes]
+    arr = (ctypes.c_int64 * max(1, len(sizes)))(*sizes)
+    a, b = _u8(a), _u8(b)
+    _cuda(c, torch.bfloat16, "c")
+    _cuda(a, torch.uint8, "a")
+    _cuda(b, torch.uint8, "b")
+    _cuda(sa, torch.float32, "sa")
+    _cuda(sb, torch.float32, "sb")
+    g, m, n = c.shape
+    k_tot = a.shape[0]
+    if g != len(sizes) or sum(sizes) != k_tot or tuple(a.shape) != (k_tot, m) or tuple(b.shape) != (k_tot, n):
+        raise ValueError("shape mismatch")
+    if c.stride(2) != 1 or c.stride(0) != m * c.stride(1):
+        raise ValueError("c must be [G, M, N] with unit column stride and groups M rows apart")
+    kb = k_tot // BLOCK
+    if tuple(sa.shape) != ((m + BLOCK - 1) // BLOCK, kb) or tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
+        raise ValueError("scale shape mismatch")
+    if not (sa.is_contiguous() and sb.is_contiguous()):
+        raise ValueError("scales must be contiguous")
+    st = lib().dg_fp8_k_grouped_gemm_tn(ctypes.c_void_p(c.data_ptr()), int(c.stride(1)),
+                                        ctypes.c_void_p(a.data_ptr()), _ld(a, "a"), ctypes.c_void_p(sa.data_ptr()),
+                                        ctypes.c_void_p(b.data_ptr()), _ld(b, "b"), ctypes.c_void_p(sb.data_ptr()),
+                                        len(sizes), arr, m, n, int(scale_mode), _stream(c))
+    _check(st, "dg_fp8_k_grouped_gemm_tn")
     return c
 
 

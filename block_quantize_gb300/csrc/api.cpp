@@ -46,9 +46,11 @@ int check_device() {
 // nothing to do (M or N is 0: every pointer may then be NULL), else an error.
 constexpr int kEmpty = -1;
 
-int validate_gemm_common(const void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
-                         const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
-                         int64_t K, int scale_mode) {
+// a_row / b_row: the row length the operand's storage needs (K for K-major
+// operands, M or N for MN-major ones).
+int validate_gemm_rows(const void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                       const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
+                       int scale_mode, int64_t a_row, int64_t b_row) {
   if (M < 0 || N < 0 || K < 0) return DG_ERR_INVALID_ARG;
   if (scale_mode != DG_SCALE_FP32 && scale_mode != DG_SCALE_UE8M0) return DG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return kEmpty;
@@ -59,12 +61,18 @@ int validate_gemm_common(const void* c, int64_t ld_c, const uint8_t* a, int64_t 
   if (!aligned(c, 16) || ld_c % 8 != 0) return DG_ERR_MISALIGNED;
   if (K == 0) return DG_OK;  // C = 0; the operands are not read
   if (!a || !b || !sa || !sb) return DG_ERR_INVALID_ARG;
-  if (ld_a < K || ld_b < K) return DG_ERR_INVALID_ARG;
+  if (ld_a < a_row || ld_b < b_row) return DG_ERR_INVALID_ARG;
   if (ld_a >= kDimLimit || ld_b >= kDimLimit) return DG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(a, 16) || !aligned(b, 16) || !aligned(sa, 4) || !aligned(sb, 4))
     return DG_ERR_MISALIGNED;
   if (ld_a % 16 != 0 || ld_b % 16 != 0) return DG_ERR_MISALIGNED;
   return DG_OK;
+}
+
+int validate_gemm_common(const void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                         const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
+                         int64_t K, int scale_mode) {
+  return validate_gemm_rows(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, K, K);
 }
 
 // C = 0 when the K extent is empty.
@@ -211,6 +219,7 @@ static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, con
   p.num_sms_cap = g_num_sms_cap.load();
   p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
   p.sa_per_row = a_1x128;
+  p.ld_sa = p.ld_sb = K / 128;
   return dg::launch_gemm(p, st);
 }
 
@@ -273,6 +282,7 @@ static int gemm_grouped(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, c
   p.num_sms_cap = g_num_sms_cap.load();
   p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
   p.sa_per_row = a_1x128;
+  p.ld_sa = p.ld_sb = K / 128;
   return dg::launch_gemm(p, st);
 }
 
@@ -306,6 +316,96 @@ DG_API int dg_fp8_grouped_gemm_contiguous_requant(uint8_t* cq, int64_t ld_cq, fl
   }
   return gemm_grouped(cq, ld_cq, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
                       a_scale_rows == 1, make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
+}
+
+DG_API int dg_fp8_gemm(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                       const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
+                       int layout, int scale_mode, void* stream) {
+  if (layout < DG_LAYOUT_NT || layout > DG_LAYOUT_TT) return DG_ERR_INVALID_ARG;
+  const bool a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
+  const bool b_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_NN;
+  const int v = validate_gemm_rows(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, a_mn ? M : K,
+                                   b_mn ? N : K);
+  if (v == kEmpty) return DG_OK;
+  if (v != DG_OK) return v;
+  const int dev_st = check_device();
+  if (dev_st != DG_OK) return dev_st;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(c, ld_c, M, N, st);
+  dg::GemmProblem p{};
+  p.c = c;
+  p.ld_c = ld_c;
+  p.a = a;
+  p.ld_a = ld_a;
+  p.sa = sa;
+  p.b = b;
+  p.ld_b = ld_b;
+  p.sb = sb;
+  p.num_groups = 1;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_sms_cap = g_num_sms_cap.load();
+  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.ld_sa = p.ld_sb = K / 128;
+  return dg::launch_gemm(p, st);
+}
+
+DG_API int dg_fp8_k_grouped_gemm_tn(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
+                                    const uint8_t* b, int64_t ld_b, const float* sb, int num_groups,
+                                    const int64_t* k_sizes, int64_t M, int64_t N, int scale_mode,
+                                    void* stream) {
+  if (num_groups < 1 || !k_sizes) return DG_ERR_INVALID_ARG;
+  int64_t k_tot = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    if (k_sizes[g] < 0) return DG_ERR_INVALID_ARG;
+    if (k_sizes[g] % 128 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    k_tot += k_sizes[g];
+    if (k_tot >= kDimLimit) return DG_ERR_UNSUPPORTED_SHAPE;
+  }
+  const int v = validate_gemm_rows(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, k_tot, scale_mode, M, N);
+  if (v == kEmpty) return DG_OK;
+  if (v != DG_OK) return v;
+  if (static_cast<int64_t>(num_groups) * M >= kDimLimit) return DG_ERR_UNSUPPORTED_SHAPE;
+  const int dev_st = check_device();
+  if (dev_st != DG_OK) return dev_st;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* c16 = static_cast<uint16_t*>(c);
+  int64_t k_off = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    void* cg = c16 + static_cast<int64_t>(g) * M * ld_c;
+    const int64_t kg = k_sizes[g];
+    int r;
+    if (kg == 0) {
+      r = zero_output(cg, ld_c, M, N, st);
+    } else {
+      // Group g: C_g = A[k_off : k_off + kg]^T B[k_off : k_off + kg] with its K blocks' scales.
+      dg::GemmProblem p{};
+      p.c = cg;
+      p.ld_c = ld_c;
+      p.a = a + k_off * ld_a;
+      p.ld_a = ld_a;
+      p.sa = sa + k_off / 128;
+      p.b = b + k_off * ld_b;
+      p.ld_b = ld_b;
+      p.sb = sb + k_off / 128;
+      p.num_groups = 1;
+      p.M = M;
+      p.N = N;
+      p.K = kg;
+      p.num_sms_cap = g_num_sms_cap.load();
+      p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+      p.a_mn = true;
+      p.b_mn = true;
+      p.ld_sa = p.ld_sb = k_tot / 128;
+      r = dg::launch_gemm(p, st);
+    }
+    if (r != DG_OK) return r;
+    k_off += kg;
+  }
+  return DG_OK;
 }
 
 DG_API int dg_get_device_status(void* stream) {

@@ -116,6 +116,12 @@ __device__ __forceinline__ uint64_t f32x2(uint32_t lo, uint32_t hi) {
 __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t s2, uint64_t p2) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(s2), "l"(p2));
 }
+// Two FP32 products in one instruction, each rounded to nearest.
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float2 f32x2_split(uint64_t v) {
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
@@ -422,11 +428,54 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// Descriptor of an MN-major 8-bit operand tile: rows are K indices, each row
+// holds mn_bytes (128 or 64) consecutive M (or N) elements, rows swizzled in
+// groups of 8 (128- or 64-byte swizzle, as TMA writes them). For MN-major
+// layouts the stride-dimension offset is the step between 8-row groups along
+// K and the leading-dimension offset the step between swizzle-atom columns
+// along MN (checked on the GPU with one MMA per variant against a host
+// product). Atom columns of a 256-wide tile sit 16 KB apart (128 rows each).
+__device__ __forceinline__ uint64_t mn_major_desc(uint32_t saddr, uint32_t mn_bytes) {
+  const uint32_t sbo = mn_bytes * 8;  // one 8-row group
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(16384u >> 4) << 16;
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(mn_bytes == 128 ? 2u : 4u) << 61;  // 128- or 64-byte swizzle
+  return d;
+}
+
+// How one operand's K-block tile sits in shared memory, and how its
+// descriptor advances by one MMA (K = 32): K-major rows of 128 K bytes
+// (+32 bytes), or MN-major rows of mn_bytes (+4 groups of 8 rows).
+struct OperandTile {
+  uint32_t mn_major;  // 0 or 1
+  uint32_t mn_bytes;  // MN-major row width: 128 or 64
+  __device__ __forceinline__ uint64_t desc(uint32_t saddr) const {
+    return mn_major ? mn_major_desc(saddr, mn_bytes) : sw128_kmajor_desc(saddr);
+  }
+  __device__ __forceinline__ uint32_t kstep() const { return mn_major ? (mn_bytes * 32u) >> 4 : 2u; }
+};
+
+// TMA load of a K-block tile: K-major maps are {K, rows}, MN-major maps {rows, K}.
+__device__ __forceinline__ void tma_load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, int k0,
+                                                 int row0, uint32_t mn_major) {
+  if (mn_major)
+    tma_load_2d(dst, map, bar, row0, k0);
+  else
+    tma_load_2d(dst, map, bar, k0, row0);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: F32 accumulator
 // (bits 4-5 = 1), A and B E4M3 (bits 7-9, 10-12 = 0), both K-major
 // (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+// The transpose bits of an instruction descriptor: A (bit 15) and B (bit 16) MN-major.
+__host__ __device__ constexpr uint32_t idesc_majors(bool a_mn, bool b_mn) {
+  return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
 }
 
 }  // namespace dg

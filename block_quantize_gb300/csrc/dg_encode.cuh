@@ -83,6 +83,27 @@ __device__ __forceinline__ uint32_t encode4_any(const float4 v, float s, float r
   return encode4<2>(v, s, r);
 }
 
+// E4M3 codes of fl32(v / s) for four values held as two FP32 pairs (the
+// epilogue's accumulator layout), with the arithmetic of encode4 done in
+// packed f32x2 multiplies. r2 = (1/s, 1/s).
+__device__ __forceinline__ uint32_t encode4_pairs(uint64_t v01, uint64_t v23, float s, uint64_t r2, bool pow2) {
+  const uint64_t q01 = fmul2(v01, r2), q23 = fmul2(v23, r2);
+  const float2 a = f32x2_split(q01), b = f32x2_split(q23);
+  const uint32_t c = cvt2(a.x, a.y) | (cvt2(b.x, b.y) << 16);
+  if (pow2) return c;  // q = v / s exactly
+  if (s >= 0x1p-126f) {
+    const uint64_t lo2 = f32x2(__float_as_uint(1.0f - 0x1p-20f), __float_as_uint(1.0f - 0x1p-20f));
+    const uint64_t hi2 = f32x2(__float_as_uint(1.0f + 0x1p-20f), __float_as_uint(1.0f + 0x1p-20f));
+    const float2 la = f32x2_split(fmul2(q01, lo2)), lb = f32x2_split(fmul2(q23, lo2));
+    const float2 ha = f32x2_split(fmul2(q01, hi2)), hb = f32x2_split(fmul2(q23, hi2));
+    const uint32_t lo = cvt2(la.x, la.y) | (cvt2(lb.x, lb.y) << 16);
+    const uint32_t hi = cvt2(ha.x, ha.y) | (cvt2(hb.x, hb.y) << 16);
+    if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
+  }
+  const float2 va = f32x2_split(v01), vb = f32x2_split(v23);
+  return cvt2(va.x / s, va.y / s) | (cvt2(vb.x / s, vb.y / s) << 16);
+}
+
 // ---------------------------------------------------------------------------
 // Requantizing GEMM epilogue.
 //
@@ -102,6 +123,18 @@ __host__ __device__ constexpr uint32_t requant_xchg_bytes(int epi_warps) {
   return 2 * 8 + 2 * epi_warps * 4 + 2 * epi_warps * 32 * 4;
 }
 
+// One epilogue warp's staging box for its 32 x 64 codes (TMA store source).
+constexpr uint32_t kRequantBoxBytes = 32 * 64;
+
+// Shared memory of the requantizing epilogue: the exchange, then one
+// 1024-byte-aligned staging box per epilogue warp.
+__host__ __device__ constexpr uint32_t requant_smem_bytes(int epi_warps) {
+  return (requant_xchg_bytes(epi_warps) + 1023u) / 1024u * 1024u + epi_warps * kRequantBoxBytes;
+}
+__device__ __forceinline__ uint8_t* requant_box(uint8_t* xchg, int epi_warps, int ew) {
+  return xchg + (requant_xchg_bytes(epi_warps) + 1023u) / 1024u * 1024u + ew * kRequantBoxBytes;
+}
+
 // Initializes the two exchange barriers (one thread, before the CTA's first sync).
 __device__ __forceinline__ void requant_xchg_init(uint8_t* xchg, int epi_warps) {
   uint64_t* bar = reinterpret_cast<uint64_t*>(xchg);
@@ -109,21 +142,27 @@ __device__ __forceinline__ void requant_xchg_init(uint8_t* xchg, int epi_warps) 
   mbar_init(smem_u32(&bar[1]), epi_warps);
 }
 
-// Requantizes one thread's slice: row `row` (valid: row < M and not a padding
-// row; invalid rows count as zeros and store nothing unless store_zero_row),
-// columns [col0, col0 + 64) of an N-column output, tile sequence number tl
-// (the same for all epilogue warps of the CTA). Returns false if a wait failed
-// (abort raised or timeout); then nothing is stored.
+// Requantizes one thread's slice: row `row` = row0 + lane (valid: row < M and
+// not a padding row; invalid rows count as zeros and store nothing unless
+// store_zero_row), columns [col0, col0 + 64) of an N-column output, tile
+// sequence number tl (the same for all epilogue warps of the CTA). Whole
+// 64-column slices leave through this warp's 2 KB staging box (64-byte
+// swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)) and a TMA
+// store clipped at M; a slice that crosses column N is stored element by
+// element (the swizzled store clips N only to whole 16-byte chunks). Returns
+// false if a wait failed (abort raised or timeout); then nothing is stored.
 template <int kEpiWarps>
 __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], bool row_valid,
-                                                    bool store_zero_row, int row, int M, int N, int col0,
+                                                    bool store_zero_row, int row0, int M, int N, int col0,
                                                     int ew, int lane, uint32_t tl, uint8_t* xchg,
-                                                    const RequantOut& o, volatile int* abort,
+                                                    const RequantOut& o, const CUtensorMap* tmap_q,
+                                                    uint8_t* box, bool& stores_issued, volatile int* abort,
                                                     unsigned int* status, uint64_t limit) {
   uint64_t* bar = reinterpret_cast<uint64_t*>(xchg);
   const uint32_t p = tl & 1u;
   float* xw = reinterpret_cast<float*>(xchg + 16) + p * kEpiWarps;
   float* xv = reinterpret_cast<float*>(xchg + 16 + 2 * kEpiWarps * 4) + p * kEpiWarps * 32;
+  const int row = row0 + lane;
 
   float m = 0.f;
   if (row_valid) {
@@ -159,39 +198,48 @@ __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], b
   const float r = 1.0f / s;
   const int sblk = col0 >> 7;  // 128-column block of this slice
 
-  if (col0 < N) {
-    if (o.block_rows == 1) {
-      if ((ew & 4) == 0 && row < M && (row_valid || store_zero_row))
-        o.s[static_cast<int64_t>(row) * o.ld_s + sblk] = s;
-    } else if (ew == (ew & ~7) && lane == 0 && (row & ~127) < M) {
-      // One thread per block; the block's first row is row & ~127.
-      o.s[static_cast<int64_t>(row >> 7) * o.ld_s + sblk] = s;
-    }
+  if (col0 >= N) return true;
+  if (o.block_rows == 1) {
+    if ((ew & 4) == 0 && row < M && (row_valid || store_zero_row))
+      o.s[static_cast<int64_t>(row) * o.ld_s + sblk] = s;
+  } else if (ew == (ew & ~7) && lane == 0 && (row0 & ~127) < M) {
+    // One thread per block; the block's first row is row0 & ~127.
+    o.s[static_cast<int64_t>(row0 >> 7) * o.ld_s + sblk] = s;
   }
-  if (row >= M || !(row_valid || store_zero_row) || col0 >= N) return true;
 
-  uint8_t* dst = o.q + static_cast<int64_t>(row) * o.ld_q + col0;
+  const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
   uint32_t code[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float2 a = f32x2_split(acc[2 * j]), b = f32x2_split(acc[2 * j + 1]);
-    code[j] = row_valid ? encode4_any(make_float4(a.x, a.y, b.x, b.y), s, r, pow2) : 0u;
-  }
+  for (int j = 0; j < 16; ++j) code[j] = row_valid ? encode4_pairs(acc[2 * j], acc[2 * j + 1], s, r2, pow2) : 0u;
+
   if (col0 + 64 <= N) {
+    if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
+    __syncwarp();
+    uint8_t* my_row = box + lane * 64;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
-  } else {
-    const int n = N - col0;  // 1..63 valid columns
+      *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < M) {
+      tma_store_2d(tmap_q, smem_u32(box), col0, row0);
+      bulk_commit();
+      stores_issued = true;
+    }
+    return true;
+  }
+  if (row >= M || !(row_valid || store_zero_row)) return true;
+  uint8_t* dst = o.q + static_cast<int64_t>(row) * o.ld_q + col0;
+  const int n = N - col0;  // 1..63 valid columns
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (4 * j + 3 < n) {
-        *reinterpret_cast<uint32_t*>(dst + 4 * j) = code[j];
-      } else {
+  for (int j = 0; j < 16; ++j) {
+    if (4 * j + 3 < n) {
+      *reinterpret_cast<uint32_t*>(dst + 4 * j) = code[j];
+    } else {
 #pragma unroll
-        for (int t = 0; t < 4; ++t)
-          if (4 * j + t < n) dst[4 * j + t] = static_cast<uint8_t>(code[j] >> (8 * t));
-      }
+      for (int t = 0; t < 4; ++t)
+        if (4 * j + t < n) dst[4 * j + t] = static_cast<uint8_t>(code[j] >> (8 * t));
     }
   }
   return true;

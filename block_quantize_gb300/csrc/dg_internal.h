@@ -78,6 +78,9 @@ struct GemmProblem {
   bool pow2_scales;          // every scale is a power of two (DG_SCALE_UE8M0)
   bool sa_per_row;           // sa is [M][K/128] (one A scale per row and K block)
   RequantOut rq;             // rq.q != nullptr: E4M3 output instead of bf16 c
+  bool a_mn;                 // A stored [K][ld_a] (M contiguous) instead of [M][ld_a]
+  bool b_mn;                 // B stored [K][ld_b] (N contiguous) instead of [N][ld_b]
+  int64_t ld_sa, ld_sb;      // row strides of sa and sb in floats (normally K/128)
 };
 
 // Returns a dg_status value.

@@ -70,6 +70,9 @@ struct GemmArgs {
   const int32_t* m_indices;
   int M, N;
   int num_kb;      // K / 128
+  int ld_sa, ld_sb;  // row strides of sa and sb (floats)
+  uint32_t idesc;  // MMA instruction descriptor (shape and operand majorness)
+  int a_mn, b_mn;  // MN-major A ([K][M]) / B ([K][N]) tiles
   int num_mb;      // ceil(M / 128)
   int num_nb;      // ceil(N / BN)
   int nbs;         // ceil(N / 128): rows of one expert's sb
@@ -118,7 +121,7 @@ struct Cfg {
 template <int BN, bool kQ>
 __host__ __device__ constexpr uint32_t out_bytes() {
   static_assert(!kQ || Cfg<BN>::kCols == 64, "the requantizing epilogue takes 64-column slices");
-  return kQ ? requant_xchg_bytes(Cfg<BN>::kEpiWarps) : Cfg<BN>::kOutBytes;
+  return kQ ? requant_smem_bytes(Cfg<BN>::kEpiWarps) : Cfg<BN>::kOutBytes;
 }
 
 // Output tile of persistent iteration t: grouped raster, M fastest inside a
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if (C::kTmaStore && !kQ) tma_prefetch_desc(&tmap_c);
+    if (C::kTmaStore) tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
@@ -236,11 +239,19 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           if (ok) {
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, args.a_box_bytes + C::kBTileBytes);
-            tma_load_2d(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, mb * kBM);
-            if constexpr (kGrouped)
-              tma_load_3d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN, g);
-            else
-              tma_load_2d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN);
+            tma_load_operand(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, mb * kBM,
+                             args.a_mn);
+            const uint32_t bdst = smem_u32(smem_b + stage * C::kBTileBytes);
+            if constexpr (kGrouped) {
+              tma_load_3d(bdst, &tmap_b, fb, kb * kBK, nb * BN, g);
+            } else if (args.b_mn) {
+              // MN-major B: 128-column boxes (one 128-byte swizzle atom column each), 16 KB apart.
+#pragma unroll
+              for (int h = 0; h < (BN >= 128 ? BN / 128 : 1); ++h)
+                tma_load_2d(bdst + h * 16384u, &tmap_b, fb, nb * BN + h * 128, kb * kBK);
+            } else {
+              tma_load_2d(bdst, &tmap_b, fb, kb * kBK, nb * BN);
+            }
             ++loads_issued;
           }
         }
@@ -276,12 +287,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           if (ok) {
             tc_fence_after();
             const uint32_t d = tmem_base + buf * BN;
-            const uint64_t adesc = sw128_kmajor_desc(smem_u32(smem_a + stage * args.a_stage_bytes));
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(smem_b + stage * C::kBTileBytes));
+            const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 128u};
+            const uint64_t adesc = at.desc(smem_u32(smem_a + stage * args.a_stage_bytes));
+            const uint64_t bdesc = bt.desc(smem_u32(smem_b + stage * C::kBTileBytes));
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k) {
-              // 32 E4M3 values = 32 bytes further along the swizzled row: +2 in addr>>4.
-              mma_e4m3(d, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+              // K-major: 32 E4M3 values = 32 bytes further along the swizzled row;
+              // MN-major: four 8-row groups further.
+              mma_e4m3(d, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc, k > 0 ? 1u : 0u);
             }
             mma_commit(smem_u32(&empty_bar[stage]));
             mma_commit(smem_u32(&tfull_bar[buf]));
@@ -319,9 +332,9 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       const int sb_block = min(col0 / kBK, args.nbs - 1);
       // This thread's row's scales (rows past M read the last row's).
       const float* sa_row =
-          args.sa + static_cast<int64_t>(args.sa_per_row ? min(mb * kBM + row_in_tile, args.M - 1) : mb) * args.num_kb;
+          args.sa + static_cast<int64_t>(args.sa_per_row ? min(mb * kBM + row_in_tile, args.M - 1) : mb) * args.ld_sa;
       const float* sb_row =
-          args.sb + (static_cast<int64_t>(g) * args.nbs + sb_block) * args.num_kb;
+          args.sb + (static_cast<int64_t>(g) * args.nbs + sb_block) * args.ld_sb;
 
       // FP32 accumulators, two columns per 64-bit register (f32x2 FMA).
       uint64_t acc[kCols / 2];
@@ -409,8 +422,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       if constexpr (kGrouped) zero_row = zero_row || (row < args.M && __ldg(args.m_indices + row) < 0);
       if constexpr (kQ) {
         // Padding rows of the grouped layout are written as zeros (scale 1).
-        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M && !zero_row, kGrouped, row, args.M, args.N, col0,
-                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit)) {
+        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M && !zero_row, kGrouped, mb * kBM + lg * 32, args.M,
+                                               args.N, col0, ew, lane, tl, smem_out, args.rq, &tmap_c,
+                                               requant_box(smem_out, C::kEpiWarps, ew), stores_issued, abort_flag,
+                                               status, limit)) {
           ok = false;
           break;
         }
@@ -489,7 +504,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         }
       }
     }
-    if (C::kTmaStore && !kQ && lane == 0 && stores_issued) bulk_wait_all();
+    if (C::kTmaStore && lane == 0 && stores_issued) bulk_wait_all();
     __syncwarp();
   }
 
@@ -631,13 +646,19 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   args.M = static_cast<int>(p.M);
   args.N = static_cast<int>(p.N);
   args.num_kb = static_cast<int>(p.K / kBK);
+  args.ld_sa = static_cast<int>(p.ld_sa);
+  args.ld_sb = static_cast<int>(p.ld_sb);
+  args.a_mn = p.a_mn ? 1 : 0;
+  args.b_mn = p.b_mn ? 1 : 0;
+  args.idesc = Cf::kIdesc | idesc_majors(p.a_mn, p.b_mn);
+  if (p.b_mn && (BN < 128 || kGrouped)) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
   args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
   // A box: all 128 rows, or the valid rows (multiple of 8) when M is small.
-  const uint32_t a_rows = p.M >= kBM ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
+  const uint32_t a_rows = (p.M >= kBM || p.a_mn) ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
   args.a_box_bytes = a_rows * kBK;
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
   const uint32_t stage_bytes = args.a_stage_bytes + Cf::kBTileBytes;
@@ -662,7 +683,13 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap ta, tb, tc;
-  {
+  if (p.a_mn) {
+    // A as [K][ld_a]: 128 (M) x 128 (K) boxes.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.M), static_cast<cuuint64_t>(p.K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_a)};
+    const cuuint32_t box[2] = {kBM, kBK};
+    if (!encode_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box)) return DG_ERR_CUDA;
+  } else {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_a)};
     const cuuint32_t box[2] = {kBK, a_rows};
@@ -675,13 +702,26 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
                                    static_cast<cuuint64_t>(p.K) * static_cast<cuuint64_t>(p.N)};
     const cuuint32_t box[3] = {kBK, static_cast<cuuint32_t>(BN), 1};
     if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, dims, strides, box)) return DG_ERR_CUDA;
+  } else if (p.b_mn) {
+    // B as [K][ld_b]: 128 (N) x 128 (K) boxes.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_b)};
+    const cuuint32_t box[2] = {128, kBK};
+    if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
   } else {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(p.N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_b)};
     const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(BN)};
     if (!encode_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box)) return DG_ERR_CUDA;
   }
-  if (Cf::kTmaStore && !kQ) {
+  if (kQ) {
+    // E4M3 codes [M][ld_q]: 64 x 32 boxes, 64-byte swizzle.
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.rq.ld_q)};
+    const cuuint32_t box[2] = {64, 32};
+    if (!encode_map(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.rq.q, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
+  } else if (Cf::kTmaStore) {
     // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.N), static_cast<cuuint64_t>(p.M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.ld_c) * 2};
@@ -690,7 +730,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
                     CU_TENSOR_MAP_SWIZZLE_64B))
       return DG_ERR_CUDA;
   } else {
-    tc = ta;  // not read by narrow tiles or the requantizing epilogue
+    tc = ta;  // not read by narrow tiles
   }
 
   auto kernel = fp8_gemm_kernel<BN, kGrouped, kQ>;
@@ -777,7 +817,8 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
       return grouped ? run_gemm<128, true, true>(p, stream, dev, sms) : run_gemm<128, false, true>(p, stream, dev, sms);
     return grouped ? run_gemm<256, true, true>(p, stream, dev, sms) : run_gemm<256, false, true>(p, stream, dev, sms);
   }
-  const int bn = pick_bn(p.M, p.N, sms);
+  int bn = pick_bn(p.M, p.N, sms);
+  if (p.b_mn && bn < 128) bn = 128;  // MN-major B tiles are whole 128-column swizzle atoms
   switch (bn) {
     case 16: return grouped ? run_gemm<16, true, false>(p, stream, dev, sms) : run_gemm<16, false, false>(p, stream, dev, sms);
     case 32: return grouped ? run_gemm<32, true, false>(p, stream, dev, sms) : run_gemm<32, false, false>(p, stream, dev, sms);

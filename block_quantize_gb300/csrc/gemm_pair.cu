@@ -72,7 +72,7 @@ struct PCfg {
   // bf16 output: staging boxes for the TMA stores; E4M3 output: the slices'
   // maxima exchange (codes are stored straight from registers).
   static constexpr uint32_t kOutBytes =
-      kQ ? requant_xchg_bytes(kEpiWarps) : kEpiWarps * kBoxBytes * (kEpiCols / 32);
+      kQ ? requant_smem_bytes(kEpiWarps) : kEpiWarps * kBoxBytes * (kEpiCols / 32);
   static_assert(!kQ || kEpiCols == 64, "the requantizing epilogue takes 64-column slices");
   static_assert(kEpiCols == 32 || kEpiCols == 64, "epilogue slice");
   static_assert(kThreads <= 1024, "CTA size");
@@ -89,6 +89,9 @@ struct PairArgs {
   unsigned int* status;
   int M, N;
   int num_kb;   // K / 128
+  int ld_sa, ld_sb;  // row strides of sa and sb (floats)
+  uint32_t idesc;    // MMA instruction descriptor (shape, scale type, operand majorness)
+  int a_mn, b_mn;    // MN-major A ([K][M]) / B ([K][N]) tiles
   int num_mb;   // ceil(M / 128)
   int num_pm;   // ceil(M / 256)
   int num_nb;   // ceil(N / 128)
@@ -145,8 +148,15 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
       if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
       const uint32_t fb = leader_full + stage * 8u;
       const uint32_t dst = ring0 + stage * kStageBytes;
-      tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
-      tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
+      // K-major maps are {K, rows}; MN-major maps {rows, K} (the tile's K rows hold 128 or 64 bytes).
+      if (args.a_mn)
+        tma_load_2d_pair(dst, &tmap_a, fb, arow, kb * kBK);
+      else
+        tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
+      if (args.b_mn)
+        tma_load_2d_pair(dst + kABytes, &tmap_b, fb, brow, kb * kBK);
+      else
+        tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
       ++issued;
       if (++stage == static_cast<uint32_t>(S)) {
         stage = 0;
@@ -252,7 +262,7 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if constexpr (!kQ) tma_prefetch_desc(&tmap_c);
+    tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kNumBuf * kBN);
   tc_fence_before();
@@ -282,18 +292,20 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
       const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
       const uint32_t tfull0 = smem_u32(tfull_bar), tempty0 = smem_u32(tempty_bar);
       const uint32_t ring0 = smem_u32(ring);
+      // A tiles: 128 rows; B tiles: this CTA's 64 of the pair's 128 columns.
+      const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 64u};
       uint32_t stage = me, sphase = 0, buf = me, bphase = 0;
       for (uint32_t it = me; it < total; it += kIssuers) {
         if (!mbar_wait(tempty0 + buf * 8u, bphase ^ 1u, abort_flag, status, limit)) break;
         if (!mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit)) break;
         tc_fence_after();
         const uint32_t base = ring0 + stage * kStageBytes;
-        const uint64_t adesc = sw128_kmajor_desc(base);
-        const uint64_t bdesc = sw128_kmajor_desc(base + kABytes);
+        const uint64_t adesc = at.desc(base);
+        const uint64_t bdesc = bt.desc(base + kABytes);
         const uint32_t d = tmem_base + buf * kBN;
 #pragma unroll
         for (int k = 0; k < kBK / 32; ++k)
-          mma_e4m3_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+          mma_e4m3_pair(d, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc, k > 0 ? 1u : 0u);
         mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
         mma_commit_pair_mc(tfull0 + buf * 8u, 0x3);
         stage += kIssuers;
@@ -328,8 +340,8 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
       // This thread's row's scales (rows past M read the last row's).
       const int arow = min(pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32 + lane, args.M - 1);
-      const float* sa_p = args.sa + static_cast<int64_t>(args.sa_per_row ? arow : mb) * args.num_kb;
-      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.num_kb;
+      const float* sa_p = args.sa + static_cast<int64_t>(args.sa_per_row ? arow : mb) * args.ld_sa;
+      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.ld_sb;
       uint64_t acc[EC / 2];  // FP32 accumulators, two columns per register pair
 #pragma unroll
       for (int j = 0; j < EC / 2; ++j) acc[j] = 0ull;
@@ -366,9 +378,10 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
 
       const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
       if constexpr (kQ) {
-        const int row = row0 + lane;
-        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, row, args.M, args.N, nb * kBN + part * EC,
-                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit)) {
+        if (!requant_store_slice<C::kEpiWarps>(acc, row0 + lane < args.M, false, row0, args.M, args.N,
+                                               nb * kBN + part * EC, ew, lane, tl, smem_out, args.rq, &tmap_c,
+                                               requant_box(smem_out, C::kEpiWarps, ew), stores_issued, abort_flag,
+                                               status, limit)) {
           ok = false;
           break;
         }
@@ -453,7 +466,7 @@ constexpr int kNatEpiWarps = 8;                        // 4 quadrants x 2 slices
 constexpr int kNatFirstEpiWarp = 8;
 constexpr int kNatThreads = 32 * (kNatFirstEpiWarp + kNatEpiWarps);
 __host__ __device__ constexpr uint32_t nat_out_bytes(bool requant) {
-  return requant ? requant_xchg_bytes(kNatEpiWarps) : kNatEpiWarps * kBoxBytes * 2;
+  return requant ? requant_smem_bytes(kNatEpiWarps) : kNatEpiWarps * kBoxBytes * 2;
 }
 static_assert(kAccCols + kNatMaxStages * kNatKbPerStage * kSfCols <= 512, "TMEM");
 
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kNatThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
-    if constexpr (!kQ) tma_prefetch_desc(&tmap_c);
+    tma_prefetch_desc(&tmap_c);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), 512);
   tc_fence_before();
@@ -543,8 +556,16 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kNatStageBytes);
           const uint32_t fb = leader_full + stage * 8u;
           const uint32_t dst = ring0 + stage * kNatStageBytes;
-          tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * kNatKbPerStage);
-          tma_load_3d_pair(dst + kNatAStageBytes, &tmap_b, fb, 0, brow, sl * kNatKbPerStage);
+          // K-major: 3-D maps {128, rows, K/128}; MN-major: 2-D maps {rows, K}
+          // whose 256-row boxes stack the stage's two K blocks.
+          if (args.a_mn)
+            tma_load_2d_pair(dst, &tmap_a, fb, arow, sl * kNatKbPerStage * kBK);
+          else
+            tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * kNatKbPerStage);
+          if (args.b_mn)
+            tma_load_2d_pair(dst + kNatAStageBytes, &tmap_b, fb, brow, sl * kNatKbPerStage * kBK);
+          else
+            tma_load_3d_pair(dst + kNatAStageBytes, &tmap_b, fb, 0, brow, sl * kNatKbPerStage);
           ++loads_issued;
           stage += 2;
           if (stage >= static_cast<uint32_t>(S)) {
@@ -562,6 +583,7 @@ __global__ void __launch_bounds__(kNatThreads, 1)
       const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
       const uint32_t ring0 = smem_u32(ring);
       uint32_t g = 0, stage = me, sphase = 0, tl = 0;  // this issuer's stages: index parity me
+      const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 64u};
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
         const uint32_t abuf = tl & 1u;
@@ -592,12 +614,12 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           for (int j = 0; j < kNatKbPerStage; ++j) {
             const int kb = sl * kNatKbPerStage + j;
             if (kb < args.num_kb) {
-              const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
-              const uint64_t bdesc = sw128_kmajor_desc(base + kNatAStageBytes + j * kBHalfBytes);
+              const uint64_t adesc = at.desc(base + j * kABytes);
+              const uint64_t bdesc = bt.desc(base + kNatAStageBytes + j * kBHalfBytes);
               const uint32_t sfa = tmem_base + kAccCols + (stage * kNatKbPerStage + j) * kSfCols;
 #pragma unroll
               for (int k = 0; k < kBK / 32; ++k)
-                mma_e4m3_pair_scaled(d, adesc + 2u * k, bdesc + 2u * k, kIdescScaled, sfa, sfa + 4,
+                mma_e4m3_pair_scaled(d, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc, sfa, sfa + 4,
                                      (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
@@ -624,8 +646,8 @@ __global__ void __launch_bounds__(kNatThreads, 1)
       int pm, nb;
       pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
-      const float* sa_p = args.sa + static_cast<int64_t>(mb) * args.num_kb;
-      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.num_kb;
+      const float* sa_p = args.sa + static_cast<int64_t>(mb) * args.ld_sa;
+      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.ld_sb;
       for (int sl = 0; sl < nst; ++sl) {
         const int kb0 = sl * kNatKbPerStage;
         const bool two = kb0 + 1 < args.num_kb;
@@ -681,9 +703,10 @@ __global__ void __launch_bounds__(kNatThreads, 1)
       for (int j = 0; j < 32; ++j) acc[j] = f32x2(r[2 * j], r[2 * j + 1]);
       const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
       if constexpr (kQ) {
-        const int row = row0 + lane;
-        if (!requant_store_slice<kNatEpiWarps>(acc, row < args.M, false, row, args.M, args.N, nb * kBN + part * 64,
-                                               ew, lane, tl, smem_out, args.rq, abort_flag, status, limit))
+        if (!requant_store_slice<kNatEpiWarps>(acc, row0 + lane < args.M, false, row0, args.M, args.N,
+                                               nb * kBN + part * 64, ew, lane, tl, smem_out, args.rq, &tmap_c,
+                                               requant_box(smem_out, kNatEpiWarps, ew), stores_issued, abort_flag,
+                                               status, limit))
           break;
       } else {
         store_tile_rows<64>(acc, tmap_c, args, out_box, row0, nb * kBN + part * 64, lane, stores_issued);
@@ -819,6 +842,11 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   args.M = static_cast<int>(p.M);
   args.N = static_cast<int>(p.N);
   args.num_kb = static_cast<int>(p.K / kBK);
+  args.ld_sa = static_cast<int>(p.ld_sa);
+  args.ld_sb = static_cast<int>(p.ld_sb);
+  args.a_mn = p.a_mn ? 1 : 0;
+  args.b_mn = p.b_mn ? 1 : 0;
+  args.idesc = (scaled ? kIdescScaled : kIdesc) | idesc_majors(p.a_mn, p.b_mn);
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_pm = static_cast<int>((p.M + 2 * kBM - 1) / (2 * kBM));
   args.num_nb = static_cast<int>((p.N + kBN - 1) / kBN);
@@ -840,6 +868,23 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   if (pairs < 1) return DG_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap ta, tb, tc;
+  const uint32_t kbs = static_cast<uint32_t>(kind.kb_per_stage);
+  if (p.a_mn) {
+    // A as [K][ld_a]: 128 (M) x 128 kb_per_stage (K) boxes, 128-byte swizzle.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K)};
+    const uint64_t str[1] = {static_cast<uint64_t>(p.ld_a)};
+    const uint32_t box[2] = {kBM, kBK * kbs};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, str, box, true)) return DG_ERR_CUDA;
+  }
+  if (p.b_mn) {
+    // B as [K][ld_b]: 64 (N) x 128 kb_per_stage (K) boxes, 64-byte swizzle.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K)};
+    const uint64_t str[1] = {static_cast<uint64_t>(p.ld_b)};
+    const uint32_t box[2] = {kBN / 2, kBK * kbs};
+    if (!encode_tensor_map_swizzle(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, str, box,
+                                   CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
+  }
   if (kind.kb_per_stage == 1) {
     const uint64_t adims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
     const uint64_t astr[1] = {static_cast<uint64_t>(p.ld_a)};
@@ -847,24 +892,29 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
     const uint64_t bdims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t bstr[1] = {static_cast<uint64_t>(p.ld_b)};
     const uint32_t bbox[2] = {kBK, kBN / 2};
-    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, adims, astr, abox, true) ||
-        !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, bdims, bstr, bbox, true))
+    if ((!p.a_mn && !encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, adims, astr, abox, true)) ||
+        (!p.b_mn && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, bdims, bstr, bbox, true)))
       return DG_ERR_CUDA;
   } else {
     // [K/128][rows][128 bytes]: one box carries kb_per_stage K blocks.
-    const uint32_t kbs = static_cast<uint32_t>(kind.kb_per_stage);
     const uint64_t adims[3] = {kBK, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K / kBK)};
     const uint64_t astr[2] = {static_cast<uint64_t>(p.ld_a), kBK};
     const uint32_t abox[3] = {kBK, kBM, kbs};
     const uint64_t bdims[3] = {kBK, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K / kBK)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(p.ld_b), kBK};
     const uint32_t bbox[3] = {kBK, kBN / 2, kbs};
-    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 3, adims, astr, abox, true) ||
-        !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true))
+    if ((!p.a_mn && !encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 3, adims, astr, abox, true)) ||
+        (!p.b_mn && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true)))
       return DG_ERR_CUDA;
   }
   if (requant) {
-    tc = ta;  // not read: the requantizing epilogue stores from registers
+    // E4M3 codes [M][ld_q]: 64 x 32 boxes, 64-byte swizzle.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.rq.ld_q)};
+    const uint32_t box[2] = {64, 32};
+    if (!encode_tensor_map_swizzle(&tc, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.rq.q, 2, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
   } else {
     // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};

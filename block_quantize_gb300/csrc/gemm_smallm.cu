@@ -75,6 +75,9 @@ struct SmallArgs {
   unsigned int* status;
   int M, N;
   int num_kb, num_nb, nbs;
+  int ld_sa, ld_sb;   // row strides of sa and sb (floats)
+  uint32_t idesc;     // MMA instruction descriptor (shape and operand majorness)
+  int a_mn, b_mn;     // MN-major A ([K][M]) / B ([K][N]) tiles
   int split;          // cluster size = number of K ranges
   int num_clusters;   // persistent clusters (grid = num_clusters * split)
   int num_stages;
@@ -183,8 +186,16 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
           if (ok) {
             const uint32_t fb = smem_u32(&full_bar[stage]);
             mbar_arrive_expect_tx(fb, args.a_box_bytes + C::kBTileBytes);
-            tma_load_2d(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, 0);
-            tma_load_2d(smem_u32(smem_b + stage * C::kBTileBytes), &tmap_b, fb, kb * kBK, nb * BN);
+            tma_load_operand(smem_u32(smem_a + stage * args.a_stage_bytes), &tmap_a, fb, kb * kBK, 0, args.a_mn);
+            const uint32_t bdst = smem_u32(smem_b + stage * C::kBTileBytes);
+            if (args.b_mn) {
+              // MN-major B: 128-column boxes (one 128-byte swizzle atom column each), 16 KB apart.
+#pragma unroll
+              for (int h = 0; h < BN / 128; ++h)
+                tma_load_2d(bdst + h * 16384u, &tmap_b, fb, nb * BN + h * 128, kb * kBK);
+            } else {
+              tma_load_2d(bdst, &tmap_b, fb, kb * kBK, nb * BN);
+            }
             ++loads_issued;
           }
         }
@@ -210,11 +221,13 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
                mbar_wait(smem_u32(&full_bar[stage]), par, abort_flag, status, limit);
           if (ok) {
             tc_fence_after();
-            const uint64_t adesc = sw128_kmajor_desc(smem_u32(smem_a + stage * args.a_stage_bytes));
-            const uint64_t bdesc = sw128_kmajor_desc(smem_u32(smem_b + stage * C::kBTileBytes));
+            const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 128u};
+            const uint64_t adesc = at.desc(smem_u32(smem_a + stage * args.a_stage_bytes));
+            const uint64_t bdesc = bt.desc(smem_u32(smem_b + stage * C::kBTileBytes));
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k)
-              mma_e4m3(tmem_base + buf * BN, adesc + 2u * k, bdesc + 2u * k, C::kIdesc, k > 0 ? 1u : 0u);
+              mma_e4m3(tmem_base + buf * BN, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc,
+                       k > 0 ? 1u : 0u);
             mma_commit(smem_u32(&empty_bar[stage]));
             mma_commit(smem_u32(&tfull_bar[buf]));
           }
@@ -238,14 +251,14 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
     const int groups8 = (col_hi - col_lo) / 8;
     const int work = args.M * groups8;
     // Offset of this thread's row's scales (rows past M read the last row's).
-    const int sa_off = args.sa_per_row ? min(row, args.M - 1) * args.num_kb : 0;
+    const int sa_off = args.sa_per_row ? min(row, args.M - 1) * args.ld_sa : 0;
     uint32_t it = 0;
     uint32_t tile_seq = 0;
     bool ok = true;
     for (int nb = cluster_id; nb < args.num_nb && ok; nb += args.num_clusters, ++tile_seq) {
       const int colt = nb * BN + grp * 64;
       const bool valid = colt < args.N;
-      const float* sb_row = args.sb + static_cast<int64_t>(min(colt / kBK, args.nbs - 1)) * args.num_kb;
+      const float* sb_row = args.sb + static_cast<int64_t>(min(colt / kBK, args.nbs - 1)) * args.ld_sb;
       uint64_t acc[32];  // 64 FP32 accumulators, two per register pair
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] = 0ull;
@@ -485,20 +498,35 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
   args.num_clusters = plan.clusters;
   CUtensorMap ta, tb;
   const uint32_t a_rows = args.a_box_bytes / kBK;
-  {
+  if (p.a_mn) {
+    // A as [K][ld_a]: 128 (M, zero-filled past M) x 128 (K) boxes.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_a)};
+    const uint32_t box[2] = {kBM, kBK};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box, true))
+      return DG_ERR_CUDA;
+  } else {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_a)};
     const uint32_t box[2] = {kBK, a_rows};
     if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, strides, box, true))
       return DG_ERR_CUDA;
   }
-  {
+  if (p.b_mn) {
+    // B as [K][ld_b]: 128 (N) x 128 (K) boxes.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_b)};
+    const uint32_t box[2] = {128, kBK};
+    if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
+      return DG_ERR_CUDA;
+  } else {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_b)};
     const uint32_t box[2] = {kBK, static_cast<uint32_t>(BN)};
     if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
       return DG_ERR_CUDA;
   }
+  args.idesc = SCfg<BN>::kIdesc | idesc_majors(p.a_mn, p.b_mn);
   if (launch_kernel(fp8_gemm_splitk_kernel<BN>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
                     smem, stream, static_cast<unsigned>(args.split), ta, tb, args) != cudaSuccess) {
     cudaGetLastError();
@@ -529,10 +557,15 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
   args.M = static_cast<int>(p.M);
   args.N = static_cast<int>(p.N);
   args.num_kb = static_cast<int>(p.K / kBK);
+  args.ld_sa = static_cast<int>(p.ld_sa);
+  args.ld_sb = static_cast<int>(p.ld_sb);
+  args.a_mn = p.a_mn ? 1 : 0;
+  args.b_mn = p.b_mn ? 1 : 0;
   args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
   args.wait_limit_ns = kDefaultWaitLimitNs;
   args.m_pad = static_cast<int>((p.M + 31) / 32 * 32);
-  const uint32_t a_rows = static_cast<uint32_t>((p.M + 7) / 8 * 8);
+  // K-major A: the valid rows (a multiple of 8); MN-major A: a full 128-byte-wide box.
+  const uint32_t a_rows = p.a_mn ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
   args.a_box_bytes = a_rows * kBK;
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
 

@@ -17,7 +17,10 @@
  *   4. both GEMMs with their FP32 accumulators requantized to E4M3 codes plus
  *      block scales in the epilogue instead of rounded to bf16 (walkthrough
  *      §2.2: quantize on demand at write-back; §6: fuse the scale computation
- *      into the kernel to save a round trip through memory).
+ *      into the kernel to save a round trip through memory);
+ *   5. the dense GEMM in all four operand layouts NT, TN, NN, TT, and the
+ *      K-grouped GEMM (pzsr.cn page §3.1: from SM100 on all four layouts;
+ *      §3.2: grouping along M or along K for MoE).
  *
  * Conventions shared by every entry point:
  *   - Every data pointer is a DEVICE pointer that the caller allocated and owns;
@@ -50,7 +53,7 @@ extern "C" {
 #define DG_API __attribute__((visibility("default")))
 #endif
 
-#define DG_ABI_VERSION 3u
+#define DG_ABI_VERSION 4u
 
 typedef enum {
     DG_OK = 0,
@@ -66,6 +69,20 @@ typedef enum {
     DG_SCALE_FP32 = 0,   /* scale = fl32(max|x| / 448); 1.0 for an all-zero block */
     DG_SCALE_UE8M0 = 1   /* the FP32 scale rounded up to a power of two, >= 2^-127 */
 } dg_scale_mode;
+
+/* Operand layouts of dg_fp8_gemm, named as op(A) op(B) in C = op(A) . op(B):
+ * N = stored as the product uses it, T = stored transposed. With logical
+ * A (M x K) and B (K x N):
+ *   NT: a [M][ld_a] (K contiguous), b [N][ld_b] (K contiguous)  -- C = A . B^T, the default layout
+ *   TN: a [K][ld_a] (M contiguous), b [K][ld_b] (N contiguous)
+ *   NN: a [M][ld_a] (K contiguous), b [K][ld_b] (N contiguous)
+ *   TT: a [K][ld_a] (M contiguous), b [N][ld_b] (K contiguous) */
+typedef enum {
+    DG_LAYOUT_NT = 0,
+    DG_LAYOUT_TN = 1,
+    DG_LAYOUT_NN = 2,
+    DG_LAYOUT_TT = 3
+} dg_layout;
 
 /* Element type of a matrix handed to the row-wise quantizer. */
 typedef enum {
@@ -218,6 +235,39 @@ DG_API int dg_fp8_grouped_gemm_contiguous_requant(uint8_t *cq, int64_t ld_cq, fl
                                                   const int32_t *m_indices,
                                                   int64_t M_tot, int64_t N, int64_t K,
                                                   int scale_mode, void *stream);
+
+/* Dense GEMM in any of the four layouts (pzsr.cn page §3.1; see dg_layout):
+ *   C[m, n] = bf16( sum_kb sa[m/128, kb] * sb[n/128, kb] * sum_{k in kb} A(m, k) B(k, n) )
+ * where A(m, k) and B(k, n) are the logical elements wherever the layout
+ * stores them. The scales are per 128 x 128 block of the logical operands
+ * whatever the layout: sa [ceil(M/128)][K/128], sb [ceil(N/128)][K/128].
+ * ld_a >= K (A stored N) or >= M (A stored T); ld_b >= K (B stored T) or
+ * >= N (B stored N); every other rule is that of dg_fp8_gemm_nt, which equals
+ * this call with layout DG_LAYOUT_NT. A bad layout gives DG_ERR_INVALID_ARG. */
+DG_API int dg_fp8_gemm(void *c, int64_t ld_c,
+                       const uint8_t *a, int64_t ld_a, const float *sa,
+                       const uint8_t *b, int64_t ld_b, const float *sb,
+                       int64_t M, int64_t N, int64_t K,
+                       int layout, int scale_mode, void *stream);
+
+/* K-grouped GEMM in the TN layout (pzsr.cn page §3.2: grouping along K, the
+ * shape of MoE weight gradients): the K extent is cut into num_groups
+ * consecutive ranges, and group g gets its own output
+ *   C_g[m, n] = bf16( sum over the K blocks kb of range g of
+ *                     sa[m/128, kb] * sb[n/128, kb] * sum_{k in kb} A[k][m] B[k][n] )
+ *   c        [num_groups][M][ld_c] bf16 out (group g at c + g * M * ld_c)
+ *   a        [K_tot][ld_a] E4M3, M contiguous (ld_a >= M); sa [ceil(M/128)][K_tot/128]
+ *   b        [K_tot][ld_b] E4M3, N contiguous (ld_b >= N); sb [ceil(N/128)][K_tot/128]
+ *   k_sizes  HOST array of num_groups sizes, each >= 0 and a multiple of 128
+ *            (DG_ERR_UNSUPPORTED_SHAPE otherwise); K_tot is their sum. A group
+ *            of size 0 gets C_g = 0.
+ * Alignment rules as dg_fp8_gemm_nt. The groups run one after another on
+ * `stream`. */
+DG_API int dg_fp8_k_grouped_gemm_tn(void *c, int64_t ld_c,
+                                    const uint8_t *a, int64_t ld_a, const float *sa,
+                                    const uint8_t *b, int64_t ld_b, const float *sb,
+                                    int num_groups, const int64_t *k_sizes,
+                                    int64_t M, int64_t N, int scale_mode, void *stream);
 
 /* Synchronize `stream`, then read and clear the current device's status word.
  * Returns DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last

@@ -12,6 +12,8 @@ numpy arrays. Every function cites the page section it follows:
   max|x| / 448 in FP32, divide, round to nearest-even E4M3; §5.4 all-zero block.
 * pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析", §3.1: NT layout, FP32 or
   power-of-two (UE8M0) scales; §2.3/§3.2: M-grouped GEMM for MoE experts.
+* pzsr.cn page §3.1 (all four layouts NT, TN, NN, TT from SM100 on) and §3.2
+  (grouping along K): ``gemm_layout`` and ``k_grouped_gemm_tn``.
 * lpnh.cn walkthrough §2.2 (accumulate in FP32, quantize on demand at
   write-back) and §6 (fuse the scale computation into the kernel): the
   requantized GEMM output, ``requantize_output`` / ``gemm_nt_requant``.
@@ -270,3 +272,49 @@ def grouped_gemm_requant(qa, sa, qb, sb, m_indices, out_block_rows: int = 1, mod
     c, e = grouped_gemm_contiguous(qa, sa, qb, sb, m_indices, rows=rows, a_1x128=a_1x128)
     q, s = requantize_output(c, out_block_rows, mode)
     return q, s, c, e
+
+
+LAYOUTS = ("NT", "TN", "NN", "TT")
+
+
+def gemm_layout(qa, sa, qb, sb, layout: str, rows=None):
+    """The block-scaled GEMM C = op(A) . op(B) in one of the layouts of
+    pzsr.cn page §3.1, named op(A) op(B): A is stored [M, K] for "N" and
+    [K, M] for "T" as first letter; B is stored [N, K] for "T" and [K, N] for
+    "N" as second letter (NT is gemm_nt). Scales are per 128 x 128 block of
+    the logical operands: sa [ceil(M/128), K/128], sb [ceil(N/128), K/128].
+    By definition this is gemm_nt on the operands brought to [M, K] and
+    [N, K]. Returns (C, E)."""
+    if layout not in LAYOUTS:
+        raise ValueError(f"unknown layout {layout}")
+    a_nk = np.asarray(qa).T if layout[0] == "T" else np.asarray(qa)
+    b_nk = np.asarray(qb).T if layout[1] == "N" else np.asarray(qb)
+    return gemm_nt(np.ascontiguousarray(a_nk), sa, np.ascontiguousarray(b_nk), sb, rows=rows)
+
+
+def k_grouped_gemm_tn(qa, sa, qb, sb, k_sizes, rows=None):
+    """K-grouped GEMM (pzsr.cn page §3.2, grouping along K): with A stored
+    [K_tot, M] and B [K_tot, N], group g owns the K range of its size and gets
+    C_g = A[range]^T . B[range] with those K blocks' scales (sa [ceil(M/128),
+    K_tot/128], sb [ceil(N/128), K_tot/128]); sizes are multiples of 128 and a
+    group of size 0 gives zeros. Returns (C [G, rows, N], E)."""
+    qa = np.asarray(qa)
+    qb = np.asarray(qb)
+    k_tot, m = qa.shape
+    n = qb.shape[1]
+    sizes = [int(v) for v in k_sizes]
+    if sum(sizes) != k_tot or any(v < 0 or v % BLOCK for v in sizes):
+        raise ValueError("group sizes must be multiples of 128 summing to K_tot")
+    nr = m if rows is None else len(rows)
+    cs = np.zeros((len(sizes), nr, n))
+    es = np.zeros((len(sizes), nr, n))
+    off = 0
+    for g, kg in enumerate(sizes):
+        if kg:
+            kb0, kb1 = off // BLOCK, (off + kg) // BLOCK
+            c, e = gemm_nt(np.ascontiguousarray(qa[off:off + kg].T), np.ascontiguousarray(sa[:, kb0:kb1]),
+                           np.ascontiguousarray(qb[off:off + kg].T), np.ascontiguousarray(sb[:, kb0:kb1]),
+                           rows=rows)
+            cs[g], es[g] = c, e
+        off += kg
+    return cs, es

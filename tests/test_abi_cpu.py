@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_strings_alignment(L):
-    assert bq.dg_get_abi_version() == 3
+    assert bq.dg_get_abi_version() == 4
     assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
     for s in range(7):
         assert bq.dg_status_string(s)
@@ -179,6 +179,44 @@ def test_requant_grouped_argument_errors(L, kw, status):
     assert grouped_rq(L, **kw) == status
 
 
+def gemm_lay(L, **kw):
+    a = dict(c=P, ldc=256, a=P, lda=512, sa=P, b=P, ldb=512, sb=P, m=128, n=256, k=512, layout=0, mode=0)
+    a.update(kw)
+    return L.dg_fp8_gemm(a["c"], a["ldc"], a["a"], a["lda"], a["sa"], a["b"], a["ldb"], a["sb"], a["m"], a["n"],
+                         a["k"], a["layout"], a["mode"], None)
+
+
+def kgrouped(L, sizes=(256, 128), **kw):
+    a = dict(c=P, ldc=256, a=P, lda=128, sa=P, b=P, ldb=256, sb=P, m=128, n=256, mode=0)
+    a.update(kw)
+    arr = (ctypes.c_int64 * len(sizes))(*sizes) if sizes is not None else None
+    return L.dg_fp8_k_grouped_gemm_tn(a["c"], a["ldc"], a["a"], a["lda"], a["sa"], a["b"], a["ldb"], a["sb"],
+                                      len(sizes) if sizes is not None else 1, arr, a["m"], a["n"], a["mode"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(layout=4), bq.DG_ERR_INVALID_ARG), (dict(layout=-1), bq.DG_ERR_INVALID_ARG),
+    # TN: a is [K][ld_a >= M], b is [K][ld_b >= N]
+    (dict(layout=1, lda=64), bq.DG_ERR_INVALID_ARG), (dict(layout=1, lda=128, ldb=128), bq.DG_ERR_INVALID_ARG),
+    # NN: b is [K][ld_b >= N]; TT: a is [K][ld_a >= M]
+    (dict(layout=2, ldb=240), bq.DG_ERR_INVALID_ARG), (dict(layout=3, lda=112, ldb=512), bq.DG_ERR_INVALID_ARG),
+    (dict(layout=1, lda=136, ldb=256), bq.DG_ERR_MISALIGNED), (dict(layout=2, k=500), bq.DG_ERR_UNSUPPORTED_SHAPE),
+    (dict(layout=3, m=0), bq.DG_OK),
+])
+def test_layout_gemm_argument_errors(L, kw, status):
+    assert gemm_lay(L, **kw) == status
+
+
+@pytest.mark.parametrize("sizes,kw,status", [
+    ((256, 100), {}, bq.DG_ERR_UNSUPPORTED_SHAPE), ((256, -128), {}, bq.DG_ERR_INVALID_ARG),
+    (None, {}, bq.DG_ERR_INVALID_ARG), ((256,), dict(lda=64), bq.DG_ERR_INVALID_ARG),
+    ((256,), dict(ldb=128), bq.DG_ERR_INVALID_ARG), ((256,), dict(a=P + 8), bq.DG_ERR_MISALIGNED),
+    ((256,), dict(m=0), bq.DG_OK),
+])
+def test_k_grouped_argument_errors(L, sizes, kw, status):
+    assert kgrouped(L, sizes, **kw) == status
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_arguments_without_gpu_report_no_device(L):
     assert gemm(L) == bq.DG_ERR_NO_DEVICE
@@ -191,6 +229,9 @@ def test_valid_arguments_without_gpu_report_no_device(L):
     assert gemm_rq(L) == bq.DG_ERR_NO_DEVICE
     assert gemm_rq(L, br=128, omode=1, arows=1) == bq.DG_ERR_NO_DEVICE
     assert grouped_rq(L) == bq.DG_ERR_NO_DEVICE
+    for layout in range(4):
+        assert gemm_lay(L, layout=layout) == bq.DG_ERR_NO_DEVICE
+    assert kgrouped(L) == bq.DG_ERR_NO_DEVICE
     assert L.dg_selftest_wait_timeout(1000, None) == bq.DG_ERR_NO_DEVICE
 
 
