@@ -539,6 +539,41 @@ def run_aux(args):
             res.append({"variant": name, "M": m, "N": n, "K": k, "us": ms * 1e3, "tflops": tf,
                         "frac_fp8_burst": tf / fp8_peak})
         out["results"] = res
+    elif kind == "layouts":
+        # The same logical GEMM with A and B stored in each of the four layouts.
+        m, n, k = (int(v) for v in (spec or "4096,7168,2048").split(","))
+        qa, sa = _rand_fp8((m, k), dev, gen, 0)
+        copies = max(1, -(-3 * L2_BYTES // (n * k)))
+        bs = [_rand_fp8((n, k), dev, gen, 0) for _ in range(copies)]
+        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        res = []
+        for layout in ("NT", "TN", "NN", "TT"):
+            a_st = qa.t().contiguous() if layout[0] == "T" else qa
+            b_st = [(qb.t().contiguous() if layout[1] == "N" else qb, sb) for qb, sb in bs]
+            fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm(c, a_st, qb, sa, sb, layout) for qb, sb in b_st]
+            ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
+            tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+            res.append({"layout": layout, "M": m, "N": n, "K": k, "us": ms * 1e3, "tflops": tf,
+                        "frac_fp8_burst": tf / fp8_peak})
+            del b_st
+        out["results"] = res
+    elif kind == "kgrouped":
+        # K-grouped TN GEMM shaped like an MoE weight gradient: dW_g [N_int, hidden]
+        # = dY_g^T X_g over the tokens routed to expert g (padded to 128).
+        mo = synthetic.MOE
+        sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
+        sizes = [int(-(-int(v) // 128) * 128) for v in sizes]
+        m, n, k_tot = mo["intermediate"], mo["hidden"], sum(sizes)
+        qa, sa = _rand_fp8((m, k_tot), dev, gen, 0)
+        qb, sb = _rand_fp8((n, k_tot), dev, gen, 0)
+        a_st, b_st = qa.t().contiguous(), qb.t().contiguous()
+        c = torch.empty((len(sizes), m, n), dtype=torch.bfloat16, device=dev)
+        ms = _time_each(stream, [lambda: bq.dg_fp8_k_grouped_gemm_tn(c, a_st, b_st, sa, sb, sizes)],
+                        args.steps, args.warmup)[0]
+        fl = 2.0 * m * n * k_tot
+        out["results"] = [{"M": m, "N": n, "K_tot": k_tot, "groups": sizes, "us": ms * 1e3,
+                           "tflops": fl / (ms * 1e-3) / 1e12,
+                           "frac_fp8_burst": fl / (ms * 1e-3) / 1e12 / fp8_peak}]
     elif kind == "grouped":
         mo = synthetic.MOE
         sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
@@ -576,7 +611,7 @@ def main():
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
                         "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K] | "
-                        "requant[:M,N,K[:variant]]  "
+                        "requant[:M,N,K[:variant]] | layouts[:M,N,K] | kgrouped  "
                         "(the others print per-kernel numbers for profiling)")
     args = p.parse_args()
     if args.steps is None:
