@@ -345,8 +345,14 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
       uint64_t acc[EC / 2];  // FP32 accumulators, two columns per register pair
 #pragma unroll
       for (int j = 0; j < EC / 2; ++j) acc[j] = 0ull;
+      // Scales of K blocks kb + 1 (a1, b1) and kb + 2 (a2, b2) are loaded ahead
+      // and multiplied only when used: a product right after its loads would
+      // stall every K block on the load latency (measured: ~200 cycles).
+      const int num_kb = args.num_kb;
       float s = __ldg(sa_p) * __ldg(sb_p);
-      for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+      float a1 = num_kb > 1 ? __ldg(sa_p + 1) : 0.f, b1 = num_kb > 1 ? __ldg(sb_p + 1) : 0.f;
+      float a2 = num_kb > 2 ? __ldg(sa_p + 2) : 0.f, b2 = num_kb > 2 ? __ldg(sb_p + 2) : 0.f;
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t buf = it % kNumBuf;
         if (!ready) {
           const bool w = mbar_wait(smem_u32(&tfull_bar[buf]), (it / kNumBuf) & 1u, abort_flag, status, limit);
@@ -363,16 +369,19 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + buf * 8u);
-        // Look ahead: test the next slot's barrier and fetch its scales now, so
-        // that their latency hides behind the multiply-adds below.
+        // Look ahead: test the next slot's barrier now, so that the test's
+        // latency hides behind the multiply-adds below.
         const uint32_t nx = it + 1;
         const bool next_done = mbar_test(smem_u32(&tfull_bar[nx % kNumBuf]), (nx / kNumBuf) & 1u);
-        const float s_next = kb + 1 < args.num_kb ? __ldg(sa_p + kb + 1) * __ldg(sb_p + kb + 1) : 0.f;
         const uint64_t s2 = f32x2(__float_as_uint(s), __float_as_uint(s));
 #pragma unroll
         for (int j = 0; j < EC / 2; ++j) ffma2(acc[j], s2, f32x2(r[2 * j], r[2 * j + 1]));
         ready = __all_sync(0xFFFFFFFFu, next_done);
-        s = s_next;
+        s = a1 * b1;
+        a1 = a2;
+        b1 = b2;
+        a2 = kb + 3 < num_kb ? __ldg(sa_p + kb + 3) : 0.f;
+        b2 = kb + 3 < num_kb ? __ldg(sb_p + kb + 3) : 0.f;
       }
       if (!ok) break;
 
