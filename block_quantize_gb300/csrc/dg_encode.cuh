@@ -145,11 +145,12 @@ __device__ __forceinline__ void requant_xchg_init(uint8_t* xchg, int epi_warps) 
 // Requantizes one thread's slice: row `row` = row0 + lane (valid: row < M and
 // not a padding row; invalid rows count as zeros and store nothing unless
 // store_zero_row), columns [col0, col0 + 64) of an N-column output, tile
-// sequence number tl (the same for all epilogue warps of the CTA). Whole
-// 64-column slices leave through this warp's 2 KB staging box (64-byte
-// swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4)) and a TMA
-// store clipped at M; a slice that crosses column N is stored element by
-// element (the swizzled store clips N only to whole 16-byte chunks). Returns
+// sequence number tl (the same for all epilogue warps of the CTA). With a
+// tensor map, whole 64-column slices leave through this warp's 2 KB staging
+// box (64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r / 2) % 4))
+// and a TMA store clipped at M; without one (tmap_q == nullptr) each thread
+// stores its 64 codes directly. A slice that crosses column N is stored
+// element by element (the swizzled store clips N only to whole 16-byte chunks). Returns
 // false if a wait failed (abort raised or timeout); then nothing is stored.
 template <int kEpiWarps>
 __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], bool row_valid,
@@ -212,7 +213,7 @@ __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], b
 #pragma unroll
   for (int j = 0; j < 16; ++j) code[j] = row_valid ? encode4_pairs(acc[2 * j], acc[2 * j + 1], s, r2, pow2) : 0u;
 
-  if (col0 + 64 <= N) {
+  if (col0 + 64 <= N && tmap_q != nullptr) {
     if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
     __syncwarp();
     uint8_t* my_row = box + lane * 64;
@@ -231,6 +232,12 @@ __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], b
   }
   if (row >= M || !(row_valid || store_zero_row)) return true;
   uint8_t* dst = o.q + static_cast<int64_t>(row) * o.ld_q + col0;
+  if (col0 + 64 <= N) {  // no TMA map: four 16-byte stores (ld_q and q are 16-byte aligned)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(code[4 * c], code[4 * c + 1], code[4 * c + 2], code[4 * c + 3]);
+    return true;
+  }
   const int n = N - col0;  // 1..63 valid columns
 #pragma unroll
   for (int j = 0; j < 16; ++j) {

@@ -801,10 +801,8 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
   const int sms = device_info(dev).num_sms;
   if (sms <= 0) return DG_ERR_NO_DEVICE;
-  // Decode shapes (M <= 128) with bf16 output: cluster split-K. The
-  // requantizing epilogue needs a tile's full rows, so it takes the kernels below.
-  if (!block_n_override() && p.rq.q == nullptr && small_m_supported(p.M, p.m_indices))
-    return launch_gemm_small_m(p, stream);
+  // Decode shapes (M <= 128): cluster split-K.
+  if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
   if (!block_n_override() && p.m_indices == nullptr && p.M > kBM) {
     const int r = launch_gemm_pair(p, stream);
     if (r != DG_ERR_UNSUPPORTED_SHAPE) return r;

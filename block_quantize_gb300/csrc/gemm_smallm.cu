@@ -34,6 +34,7 @@
 
 #include "../../include/dgfp8.h"
 #include "dg_device.cuh"
+#include "dg_encode.cuh"
 #include "dg_internal.h"
 
 namespace dg {
@@ -46,6 +47,7 @@ constexpr uint32_t kATileBytes = kBM * kBK;
 constexpr size_t kMaxDynSmem = 227 * 1024;
 constexpr size_t kMinSmemPerCta = 120 * 1024;
 constexpr int kMaxSplit = 8;
+constexpr int kMaxSplitC = kMaxSplit;
 
 template <int BN>
 struct SCfg {
@@ -64,10 +66,20 @@ struct SCfg {
   static constexpr int kChunk = (kThreads > 512) ? 16 : 32;
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
   static_assert(kThreads <= 1024, "CTA size");
+  // Requantized output: 128-column blocks per tile, and the shared memory of
+  // the block-max exchange (per tile parity: the epilogue slices' exchange of
+  // a CTA that reduces alone, this CTA's partial maxima and every rank's copy
+  // of them, and two pairs of barriers).
+  static constexpr int kNBlk = BN / 128;
+  static constexpr uint32_t kRqXchg = (requant_xchg_bytes(kEpiWarps) + 15u) / 16u * 16u;
+  static constexpr uint32_t kRqPmaxWords = 2 * kBM * kNBlk;
+  static constexpr uint32_t kRqXmaxWords = 2 * kMaxSplitC * kBM * kNBlk;
+  static constexpr uint32_t kRqBytes = kRqXchg + 4 * (kRqPmaxWords + kRqXmaxWords) + 4 * 8;
 };
 
 struct SmallArgs {
   __nv_bfloat16* c;
+  RequantOut rq;      // E4M3 output (requantizing kernels)
   int sa_per_row;  // sa is [M][K/128] instead of [1][K/128]
   int64_t ld_c;
   const float* sa;
@@ -108,7 +120,129 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, int gcol, int N
   }
 }
 
+// Requantizing end of a tile for a cluster of split >= 2 CTAs. This CTA has
+// the sums of its column share; the block maxima span the cluster:
+//   1. sum this thread's items (row, 8 columns) over the peers' partials in
+//      rank order and keep them in registers (at most 4 items: work <=
+//      M * ceil(BN/8/split) <= 8 BN items over 2 BN threads), then release the
+//      peers' partial buffers (`consumed`);
+//   2. fold each item's max|v| into this CTA's maxima (shared atomicMax on the
+//      bit patterns of non-negative floats), per (row, 128-column block) or
+//      per block; wait until every epilogue warp of the CTA has folded;
+//   3. write the CTA's maxima into slot `rank` of every peer and arrive on the
+//      peer's exchange barrier (lane s -> peer s); wait on this CTA's;
+//   4. the block max is the max over the ranks' slots: scale, encode the
+//      items and store their 8 codes; rank 0 stores the scales.
+// Two parities alternate between tiles. A parity's maxima are cleared after
+// its exchange wait (every local warp has sent them by then); a peer writes a
+// parity's slot again only after the next tile's exchange, which comes after
+// this CTA's reads. Returns false if a wait failed.
 template <int BN>
+__device__ __forceinline__ bool requant_cluster_tile(const SmallArgs& args, const float* part, uint32_t rank,
+                                                     int split, int nb, int col_lo, int groups8, int work, int ew,
+                                                     int lane, uint32_t tile_seq, uint32_t* rq_pmax,
+                                                     uint32_t* rq_xmax, uint64_t* rq_bar, uint64_t* consumed_bar,
+                                                     volatile int* abort_flag, unsigned int* status,
+                                                     uint64_t limit) {
+  using C = SCfg<BN>;
+  constexpr int kNB = C::kNBlk;
+  constexpr int kT = C::kEpiWarps * 32;
+  const RequantOut& o = args.rq;
+  const bool per_row = o.block_rows == 1;
+  const uint32_t p = tile_seq & 1u;
+  const uint32_t ph = (tile_seq >> 1) & 1u;
+  uint32_t* pm = rq_pmax + p * (kBM * kNB);
+  uint32_t* xm = rq_xmax + p * (kMaxSplit * kBM * kNB);
+  const int tid = ew * 32 + lane;
+
+  float v[4][8];
+  int rr[4], col[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int g = tid + i * kT;
+    rr[i] = -1;
+    col[i] = 0;
+    if (g < work) {
+      rr[i] = g / groups8;
+      col[i] = col_lo + (g % groups8) * 8;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[i][q] = 0.f;
+      const uint32_t local = smem_u32(part + rr[i] * C::kPartStride + col[i]);
+      for (int s = 0; s < split; ++s) {
+        const uint32_t ra = mapa_shared(local, s);
+        const float4 x0 = ld_dsmem_f4(ra), x1 = ld_dsmem_f4(ra + 16);
+        v[i][0] += x0.x; v[i][1] += x0.y; v[i][2] += x0.z; v[i][3] += x0.w;
+        v[i][4] += x1.x; v[i][5] += x1.y; v[i][6] += x1.z; v[i][7] += x1.w;
+      }
+    }
+  }
+  __syncwarp();
+  if (lane < split) mbar_arrive_remote(mapa_shared(smem_u32(consumed_bar), lane));
+
+  // 2. this CTA's maxima
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (rr[i] < 0) continue;
+    float m = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(v[i][q]));
+    atomicMax(&pm[(per_row ? rr[i] : 0) * kNB + col[i] / 128], __float_as_uint(m));
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&rq_bar[2 + p]));
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&rq_bar[2 + p]), ph, abort_flag, status, limit))) return false;
+
+  // 3. send them to every rank (this one included)
+  const int entries = (per_row ? args.M : 1) * kNB;
+  for (int e = tid; e < entries * split; e += kT) {
+    const int s = e % split, ent = e / split;
+    st_dsmem_u32(mapa_shared(smem_u32(xm + static_cast<int>(rank) * (kBM * kNB) + ent), s), pm[ent]);
+  }
+  __syncwarp();
+  if (lane < split) mbar_arrive_remote(mapa_shared(smem_u32(&rq_bar[p]), lane));
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait_cluster(smem_u32(&rq_bar[p]), ph, abort_flag, status, limit)))
+    return false;
+  for (int e = tid; e < entries; e += kT) pm[e] = 0u;  // ready for tile + 2
+
+  // 4. scales, codes
+  const bool pow2 = o.pow2 != 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (rr[i] < 0) continue;
+    const int ent = (per_row ? rr[i] : 0) * kNB + col[i] / 128;
+    uint32_t am = 0u;
+    for (int s = 0; s < split; ++s) am = max(am, xm[s * (kBM * kNB) + ent]);
+    const float sc = block_scale(__uint_as_float(am), pow2);
+    const float r = 1.0f / sc;
+    const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
+    const uint32_t c0 = encode4_pairs(f32x2(__float_as_uint(v[i][0]), __float_as_uint(v[i][1])),
+                                      f32x2(__float_as_uint(v[i][2]), __float_as_uint(v[i][3])), sc, r2, pow2);
+    const uint32_t c1 = encode4_pairs(f32x2(__float_as_uint(v[i][4]), __float_as_uint(v[i][5])),
+                                      f32x2(__float_as_uint(v[i][6]), __float_as_uint(v[i][7])), sc, r2, pow2);
+    const int gcol = nb * BN + col[i];
+    uint8_t* dst = o.q + static_cast<int64_t>(rr[i]) * o.ld_q + gcol;
+    if (gcol + 8 <= args.N) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(c0, c1);  // 8-byte aligned: gcol % 8 == 0, ld_q % 16 == 0
+    } else {
+      const uint64_t cc = (static_cast<uint64_t>(c1) << 32) | c0;
+      for (int q = 0; q < 8; ++q)
+        if (gcol + q < args.N) dst[q] = static_cast<uint8_t>(cc >> (8 * q));
+    }
+  }
+  if (rank == 0) {
+    for (int e = tid; e < entries; e += kT) {
+      const int gblk = nb * kNB + e % kNB;
+      if (gblk * 128 >= args.N) continue;
+      uint32_t am = 0u;
+      for (int s = 0; s < split; ++s) am = max(am, xm[s * (kBM * kNB) + e]);
+      o.s[static_cast<int64_t>(per_row ? e / kNB : 0) * o.ld_s + gblk] = block_scale(__uint_as_float(am), pow2);
+    }
+  }
+  __syncwarp();
+  return true;
+}
+
+template <int BN, bool kQ>
 __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
     fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a,
                            const __grid_constant__ CUtensorMap tmap_b, const SmallArgs args) {
@@ -124,6 +258,13 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   if (a_read_end > off) off = a_read_end;  // an MMA reads 128 A rows from its stage
   float* part = reinterpret_cast<float*>(smem + off);
   off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  off = (off + 15) & ~static_cast<size_t>(15);
+  // Requantized output (kQ): the block-max exchange.
+  uint8_t* rq_xchg = smem + off;
+  uint32_t* rq_pmax = reinterpret_cast<uint32_t*>(rq_xchg + C::kRqXchg);  // [2][128][kNBlk]
+  uint32_t* rq_xmax = rq_pmax + C::kRqPmaxWords;                           // [2][kMaxSplit][128][kNBlk]
+  uint64_t* rq_bar = reinterpret_cast<uint64_t*>(rq_xmax + C::kRqXmaxWords);  // amax[2], lmax[2]
+  if constexpr (kQ) off += C::kRqBytes;
   off = (off + 7) & ~static_cast<size_t>(7);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
   uint64_t* full_bar = bars;
@@ -158,12 +299,22 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
     mbar_init(smem_u32(ready_bar), split * C::kEpiWarps);
     mbar_init(smem_u32(consumed_bar), split * C::kEpiWarps);
     mbar_init(smem_u32(drain_bar), C::kIssuers);
+    if constexpr (kQ) {
+      requant_xchg_init(rq_xchg, C::kEpiWarps);
+      for (int q = 0; q < 2; ++q) {
+        mbar_init(smem_u32(&rq_bar[q]), split * C::kEpiWarps);  // every rank's warps have sent their maxima
+        mbar_init(smem_u32(&rq_bar[2 + q]), C::kEpiWarps);      // this CTA's warps have folded theirs
+      }
+    }
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  if constexpr (kQ) {
+    for (uint32_t i = threadIdx.x; i < C::kRqPmaxWords; i += blockDim.x) rq_pmax[i] = 0u;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -293,6 +444,17 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
       }
       if (!ok) break;
 
+      if (split == 1 && kQ) {
+        // No peers: the epilogue slices exchange their maxima in this CTA.
+        bool unused = false;
+        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, lg * 32, args.M, args.N, colt, ew, lane,
+                                               tile_seq, rq_xchg, args.rq, nullptr, nullptr, unused, abort_flag,
+                                               status, limit)) {
+          ok = false;
+          break;
+        }
+        continue;
+      }
       if (split == 1) {
         // No peers: round this thread's row segment to bf16 and store it.
         if (row < args.M && valid) {
@@ -331,6 +493,12 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
         const bool w = mbar_wait_cluster(smem_u32(ready_bar), tile_seq & 1u, abort_flag, status, limit);
         ok = __all_sync(0xFFFFFFFFu, w);
         if (!ok) break;
+      }
+      if constexpr (kQ) {
+        ok = requant_cluster_tile<BN>(args, part, rank, split, nb, col_lo, groups8, work, ew, lane, tile_seq,
+                                      rq_pmax, rq_xmax, rq_bar, consumed_bar, abort_flag, status, limit);
+        if (!ok) break;
+        continue;
       }
       for (int g = ew * 32 + lane; g < work; g += C::kEpiWarps * 32) {
         const int rr = g / groups8;
@@ -384,16 +552,20 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   cluster_sync_all();  // no CTA leaves while a peer may still read its partial
 }
 
-// Largest number of co-resident clusters of `split` CTAs for this kernel.
-template <int BN>
+// Largest number of co-resident clusters of `split` CTAs for this kernel
+// (cached per device and split; the shared memory of one BN/kQ pair is fixed
+// by M, so the first query per shape class stands for the others).
+template <int BN, bool kQ>
 int max_active_clusters(int split, size_t smem) {
   static std::mutex mu;
   static int cache[64][kMaxSplit + 1] = {};
+  static size_t cached_smem[64][kMaxSplit + 1] = {};
   if (split < 1 || split > kMaxSplit) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev][split] == 0) {
+  if (cache[dev][split] == 0 || cached_smem[dev][split] != smem) {
+    cached_smem[dev][split] = smem;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -406,7 +578,7 @@ int max_active_clusters(int split, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = -1;
     }
@@ -423,12 +595,13 @@ struct Plan {
 
 // Launch geometry for tile width BN: shared memory, stages, and the K split
 // with the least modelled time. Returns false if BN does not fit.
-template <int BN>
+template <int BN, bool kQ>
 bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_out, Plan& plan) {
   using C = SCfg<BN>;
   args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
   const uint32_t stage_bytes = args.a_stage_bytes + C::kBTileBytes;
-  const size_t part_bytes = static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  const size_t part_bytes = (static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float) + 15) / 16 * 16 +
+                            (kQ ? C::kRqBytes : 0);
   const size_t bar_bytes = (2 * kMaxStages + 2 * C::kNumPBuf + 3) * sizeof(uint64_t) + 32;
   if (part_bytes + bar_bytes + 1024 >= kMaxDynSmem) return false;
   const size_t budget = kMaxDynSmem - 1024 - part_bytes - bar_bytes;
@@ -456,7 +629,7 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
   const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (split > args.num_kb || (BN / 8) / split < 1) break;
-    const int active = max_active_clusters<BN>(split, smem);
+    const int active = max_active_clusters<BN, kQ>(split, smem);
     if (active <= 0) continue;
     int clusters = std::min(active, args.num_nb);
     if (p.num_sms_cap > 0) clusters = std::min(clusters, std::max(1, p.num_sms_cap / split));
@@ -477,13 +650,13 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
 
 // Allows the kernel its shared memory on the current device (once per device);
 // the occupancy query of the planner needs it too.
-template <int BN>
+template <int BN, bool kQ>
 bool set_smem_attribute() {
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (attr_set.load() & (1ull << dev)) return true;
-  if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kMaxDynSmem)) != cudaSuccess) {
     cudaGetLastError();
     return false;
@@ -492,7 +665,7 @@ bool set_smem_attribute() {
   return true;
 }
 
-template <int BN>
+template <int BN, bool kQ>
 int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_t smem, const Plan& plan) {
   args.split = plan.split;
   args.num_clusters = plan.clusters;
@@ -527,12 +700,26 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
       return DG_ERR_CUDA;
   }
   args.idesc = SCfg<BN>::kIdesc | idesc_majors(p.a_mn, p.b_mn);
-  if (launch_kernel(fp8_gemm_splitk_kernel<BN>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
+  if (launch_kernel(fp8_gemm_splitk_kernel<BN, kQ>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
                     smem, stream, static_cast<unsigned>(args.split), ta, tb, args) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }
   return DG_OK;
+}
+
+// 256-column tiles (fewer, larger TMA boxes) when the partial tile fits.
+template <bool kQ>
+int plan_and_run(const GemmProblem& p, cudaStream_t stream, int sms, const SmallArgs& args) {
+  if (!set_smem_attribute<256, kQ>() || !set_smem_attribute<128, kQ>()) return DG_ERR_CUDA;
+  SmallArgs a256 = args, a128 = args;
+  size_t s256 = 0, s128 = 0;
+  Plan p256, p128;
+  const bool ok256 = plan_small_m<256, kQ>(p, sms, a256, s256, p256);
+  const bool ok128 = plan_small_m<128, kQ>(p, sms, a128, s128, p128);
+  if (ok256 && (!ok128 || p256.cost <= p128.cost)) return run_small_m<256, kQ>(p, stream, a256, s256, p256);
+  if (ok128) return run_small_m<128, kQ>(p, stream, a128, s128, p128);
+  return DG_ERR_UNSUPPORTED_SHAPE;
 }
 
 }  // namespace
@@ -568,17 +755,8 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
   const uint32_t a_rows = p.a_mn ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
   args.a_box_bytes = a_rows * kBK;
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
-
-  // 256-column tiles (fewer, larger TMA boxes) when the partial tile fits.
-  if (!set_smem_attribute<256>() || !set_smem_attribute<128>()) return DG_ERR_CUDA;
-  SmallArgs a256 = args, a128 = args;
-  size_t s256 = 0, s128 = 0;
-  Plan p256, p128;
-  const bool ok256 = plan_small_m<256>(p, sms, a256, s256, p256);
-  const bool ok128 = plan_small_m<128>(p, sms, a128, s128, p128);
-  if (ok256 && (!ok128 || p256.cost <= p128.cost)) return run_small_m<256>(p, stream, a256, s256, p256);
-  if (ok128) return run_small_m<128>(p, stream, a128, s128, p128);
-  return DG_ERR_UNSUPPORTED_SHAPE;
+  args.rq = p.rq;
+  return p.rq.q ? plan_and_run<true>(p, stream, sms, args) : plan_and_run<false>(p, stream, sms, args);
 }
 
 }  // namespace dg

@@ -44,7 +44,7 @@ def _run_dense(qa, sa, qb, sb, in_mode, block_rows, out_mode):
 
 
 # (M, N, K): M > 128 runs on CTA pairs (FP32 promotion for in_mode 0, the
-# block-scaled MMA for in_mode 1), M <= 128 on the 1-SM kernel with 128-column tiles.
+# block-scaled MMA for in_mode 1), M <= 128 on the split-K kernel.
 EXACT_SHAPES = [(256, 256, 512), (300, 200, 1024), (129, 136, 384), (1, 384, 256), (100, 300, 640)]
 
 
@@ -59,6 +59,33 @@ def test_exact_bit_identical(oracle_mod, shape, in_mode, block_rows, out_mode):
     qr, sr, _, _ = oracle_mod.gemm_nt_requant(qa, sa, qb, sb, block_rows, out_mode)
     assert np.array_equal(s, sr), f"scales differ at {np.argwhere(s != sr)[:5].tolist()}"
     assert np.array_equal(q, qr), f"codes differ at {np.argwhere(q != qr)[:5].tolist()}"
+
+
+# Decode shapes: the split-K kernel reduces over a cluster and exchanges the
+# block maxima between its CTAs (split >= 2 for these K).
+DECODE_SHAPES = [(1, 7168, 4096), (16, 2304, 8192), (128, 1152, 4096), (77, 500, 2048)]
+
+
+@pytest.mark.parametrize("out_mode", [0, 1])
+@pytest.mark.parametrize("block_rows", [1, 128])
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_exact_decode_cluster(oracle_mod, shape, block_rows, out_mode):
+    m, n, k = shape
+    qa, sa, qb, sb = _exact_operands(m, n, k, seed=m + n)
+    q, s = _run_dense(qa, sa, qb, sb, 0, block_rows, out_mode)
+    qr, sr, _, _ = oracle_mod.gemm_nt_requant(qa, sa, qb, sb, block_rows, out_mode)
+    assert np.array_equal(s, sr), f"scales differ at {np.argwhere(s != sr)[:5].tolist()}"
+    assert np.array_equal(q, qr), f"codes differ at {np.argwhere(q != qr)[:5].tolist()}"
+
+
+@pytest.mark.parametrize("block_rows", [1, 128])
+def test_random_decode_cluster(oracle_mod, block_rows):
+    m, n, k = 128, 7168, 16384
+    qa, sa, qb, sb = _random_operands(oracle_mod, m, n, k, seed=91)
+    q, s = _run_dense(qa, sa, qb, sb, 0, block_rows, 0)
+    c, mag = oracle_mod.gemm_nt(qa, sa, qb, sb)
+    assert_requant_within_bound(q, s, c, mag, block_rows, False, f"decode 128x7168x16384 rows {block_rows}",
+                                oracle_mod)
 
 
 @pytest.mark.parametrize("block_rows", [1, 128])
