@@ -460,7 +460,13 @@ struct OperandTile {
     return mn_major ? mn_major_desc(saddr, mn_bytes) : sw128_kmajor_desc(saddr);
   }
   __device__ __forceinline__ uint32_t kstep() const { return mn_major ? (mn_bytes * 32u) >> 4 : 2u; }
+  // Every field but the start address: an issue loop computes it once and
+  // ORs in each stage's address (bits 0-13, address >> 4).
+  __device__ __forceinline__ uint64_t desc_fields() const { return desc(0u); }
 };
+__device__ __forceinline__ uint64_t desc_at(uint64_t fields, uint32_t saddr) {
+  return fields | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+}
 
 // TMA load of a K-block tile: K-major maps are {K, rows}, MN-major maps {rows, K}.
 __device__ __forceinline__ void tma_load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar, int k0,

@@ -40,6 +40,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/dgfp8.h"
 #include "dg_device.cuh"
@@ -81,7 +82,6 @@ constexpr int kEpiCols = 64;
 
 struct PairArgs {
   __nv_bfloat16* c;  // bf16 output (kernels without requantization)
-  RequantOut rq;     // E4M3 output and scales (requantizing kernels)
   int64_t ld_c;
   int sa_per_row;  // sa is [M][K/128] instead of [ceil(M/128)][K/128]
   const float* sa;
@@ -98,6 +98,14 @@ struct PairArgs {
   int num_stages;
   uint64_t wait_limit_ns;
 };
+
+// Arguments of the requantizing kernels. A separate type: the extra fields in
+// the common struct changed the bf16 kernels' register allocation.
+struct PairArgsQ : PairArgs {
+  RequantOut rq;     // E4M3 output and scales
+};
+template <bool kQ>
+using PairArgsT = std::conditional_t<kQ, PairArgsQ, PairArgs>;
 
 __device__ __forceinline__ void pair_tile_coords(int t, int num_pm, int num_nb, int& pm, int& nb) {
   const int per_group = kGroupPM * num_nb;
@@ -128,6 +136,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // SM sub-partition with busy warps and each TMA issue blocks it for a few
 // hundred cycles, so stage and phase are running counters. Returns the number
 // of stages it filled.
+template <bool kNT>
 __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                                   const PairArgs& args, uint32_t ring0, uint64_t* full_bar,
                                                   uint64_t* empty_bar, uint32_t rank, int pair, int num_pairs,
@@ -149,11 +158,11 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
       const uint32_t fb = leader_full + stage * 8u;
       const uint32_t dst = ring0 + stage * kStageBytes;
       // K-major maps are {K, rows}; MN-major maps {rows, K} (the tile's K rows hold 128 or 64 bytes).
-      if (args.a_mn)
+      if (!kNT && args.a_mn)
         tma_load_2d_pair(dst, &tmap_a, fb, arow, kb * kBK);
       else
         tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
-      if (args.b_mn)
+      if (!kNT && args.b_mn)
         tma_load_2d_pair(dst + kABytes, &tmap_b, fb, brow, kb * kBK);
       else
         tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
@@ -217,11 +226,15 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
   }
 }
 
-template <int EC, bool kQ>
+// kNT: both operands K-major (the NT layout). Its instantiation keeps layout
+// handling out of the TMA and MMA issue loops, where runtime branches on the
+// layout and runtime descriptors cost ~10 % (measured); other layouts take
+// the runtime path.
+template <int EC, bool kQ, bool kNT>
 __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
-                         const __grid_constant__ CUtensorMap tmap_c, const PairArgs args) {
+                         const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ> args) {
   using C = PCfg<EC, kQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0)
-      loads_issued = pair_producer(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
+      loads_issued = pair_producer<kNT>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
                                    num_pairs, abort_flag, status);
     __syncwarp();
   } else if (warp <= kIssuers) {
@@ -294,18 +307,29 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
       const uint32_t ring0 = smem_u32(ring);
       // A tiles: 128 rows; B tiles: this CTA's 64 of the pair's 128 columns.
       const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 64u};
+      const uint64_t afields = at.desc_fields(), bfields = bt.desc_fields();
+      const uint32_t astep = at.kstep(), bstep = bt.kstep();
+      const uint32_t idesc = args.idesc;
       uint32_t stage = me, sphase = 0, buf = me, bphase = 0;
       for (uint32_t it = me; it < total; it += kIssuers) {
         if (!mbar_wait(tempty0 + buf * 8u, bphase ^ 1u, abort_flag, status, limit)) break;
         if (!mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit)) break;
         tc_fence_after();
         const uint32_t base = ring0 + stage * kStageBytes;
-        const uint64_t adesc = at.desc(base);
-        const uint64_t bdesc = bt.desc(base + kABytes);
         const uint32_t d = tmem_base + buf * kBN;
+        if constexpr (kNT) {
+          const uint64_t adesc = sw128_kmajor_desc(base);
+          const uint64_t bdesc = sw128_kmajor_desc(base + kABytes);
 #pragma unroll
-        for (int k = 0; k < kBK / 32; ++k)
-          mma_e4m3_pair(d, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kBK / 32; ++k)
+            mma_e4m3_pair(d, adesc + 2u * k, bdesc + 2u * k, kIdesc, k > 0 ? 1u : 0u);
+        } else {
+          const uint64_t adesc = desc_at(afields, base);
+          const uint64_t bdesc = desc_at(bfields, base + kABytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)
+            mma_e4m3_pair(d, adesc + astep * k, bdesc + bstep * k, idesc, k > 0 ? 1u : 0u);
+        }
         mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
         mma_commit_pair_mc(tfull0 + buf * 8u, 0x3);
         stage += kIssuers;
@@ -485,11 +509,11 @@ __device__ __forceinline__ uint32_t ue8m0_word(float s) {
   return 0x01010101u * ((__float_as_uint(s) >> 23) & 0xFFu);
 }
 
-template <bool kQ>
+template <bool kQ, bool kNT>
 __global__ void __launch_bounds__(kNatThreads, 1)
     fp8_gemm_pair_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
-                                const __grid_constant__ CUtensorMap tmap_c, const PairArgs args) {
+                                const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ> args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -567,11 +591,11 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           const uint32_t dst = ring0 + stage * kNatStageBytes;
           // K-major: 3-D maps {128, rows, K/128}; MN-major: 2-D maps {rows, K}
           // whose 256-row boxes stack the stage's two K blocks.
-          if (args.a_mn)
+          if (!kNT && args.a_mn)
             tma_load_2d_pair(dst, &tmap_a, fb, arow, sl * kNatKbPerStage * kBK);
           else
             tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * kNatKbPerStage);
-          if (args.b_mn)
+          if (!kNT && args.b_mn)
             tma_load_2d_pair(dst + kNatAStageBytes, &tmap_b, fb, brow, sl * kNatKbPerStage * kBK);
           else
             tma_load_3d_pair(dst + kNatAStageBytes, &tmap_b, fb, 0, brow, sl * kNatKbPerStage);
@@ -593,6 +617,9 @@ __global__ void __launch_bounds__(kNatThreads, 1)
       const uint32_t ring0 = smem_u32(ring);
       uint32_t g = 0, stage = me, sphase = 0, tl = 0;  // this issuer's stages: index parity me
       const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 64u};
+      const uint64_t afields = at.desc_fields(), bfields = bt.desc_fields();
+      const uint32_t astep = at.kstep(), bstep = bt.kstep();
+      const uint32_t idesc = args.idesc;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
         const uint32_t abuf = tl & 1u;
@@ -623,13 +650,22 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           for (int j = 0; j < kNatKbPerStage; ++j) {
             const int kb = sl * kNatKbPerStage + j;
             if (kb < args.num_kb) {
-              const uint64_t adesc = at.desc(base + j * kABytes);
-              const uint64_t bdesc = bt.desc(base + kNatAStageBytes + j * kBHalfBytes);
               const uint32_t sfa = tmem_base + kAccCols + (stage * kNatKbPerStage + j) * kSfCols;
+              if constexpr (kNT) {
+                const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
+                const uint64_t bdesc = sw128_kmajor_desc(base + kNatAStageBytes + j * kBHalfBytes);
 #pragma unroll
-              for (int k = 0; k < kBK / 32; ++k)
-                mma_e4m3_pair_scaled(d, adesc + at.kstep() * k, bdesc + bt.kstep() * k, args.idesc, sfa, sfa + 4,
-                                     (kb > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < kBK / 32; ++k)
+                  mma_e4m3_pair_scaled(d, adesc + 2u * k, bdesc + 2u * k, kIdescScaled, sfa, sfa + 4,
+                                       (kb > 0 || k > 0) ? 1u : 0u);
+              } else {
+                const uint64_t adesc = desc_at(afields, base + j * kABytes);
+                const uint64_t bdesc = desc_at(bfields, base + kNatAStageBytes + j * kBHalfBytes);
+#pragma unroll
+                for (int k = 0; k < kBK / 32; ++k)
+                  mma_e4m3_pair_scaled(d, adesc + astep * k, bdesc + bstep * k, idesc, sfa, sfa + 4,
+                                       (kb > 0 || k > 0) ? 1u : 0u);
+              }
             }
           }
           mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
@@ -759,35 +795,35 @@ __global__ void __launch_bounds__(kNatThreads, 1)
 
 // The two pair kernels: FP32 scales promoted in registers, or power-of-two
 // scales applied by the tensor core.
-using PairKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PairArgs);
 struct PairKind {
-  PairKernel kernel;
+  const void* kernel;
   int threads;
   size_t fixed_smem;    // output staging + barriers
   uint32_t stage_bytes;
   int max_stages;
   int kb_per_stage;
 };
-template <bool kQ>
+template <bool kQ, bool kNT>
 PairKind pair_kind_t(bool scaled) {
   using C = PCfg<kEpiCols, kQ>;
   if (scaled)
-    return {fp8_gemm_pair_scaled_kernel<kQ>, kNatThreads,
+    return {reinterpret_cast<const void*>(&fp8_gemm_pair_scaled_kernel<kQ, kNT>), kNatThreads,
             nat_out_bytes(kQ) + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, kNatStageBytes, kNatMaxStages,
             kNatKbPerStage};
-  return {fp8_gemm_pair_kernel<kEpiCols, kQ>, C::kThreads,
+  return {reinterpret_cast<const void*>(&fp8_gemm_pair_kernel<kEpiCols, kQ, kNT>), C::kThreads,
           C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
 }
-// variant = scaled + 2 * requant
+// variant = scaled + 2 * requant + 4 * NT layout
 PairKind pair_kind(int variant) {
   const bool scaled = (variant & 1) != 0;
-  return (variant & 2) ? pair_kind_t<true>(scaled) : pair_kind_t<false>(scaled);
+  if (variant & 4) return (variant & 2) ? pair_kind_t<true, true>(scaled) : pair_kind_t<false, true>(scaled);
+  return (variant & 2) ? pair_kind_t<true, false>(scaled) : pair_kind_t<false, false>(scaled);
 }
 
 // Largest number of co-resident CTA pairs of a kernel (cached per device).
 int max_active_pairs(int variant, size_t smem) {
   static std::mutex mu;
-  static int cache[64][4] = {};
+  static int cache[64][8] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -816,7 +852,7 @@ int max_active_pairs(int variant, size_t smem) {
 }
 
 bool set_pair_smem_attribute(int variant) {
-  static std::atomic<uint64_t> done[4] = {{0}, {0}, {0}, {0}};
+  static std::atomic<uint64_t> done[8] = {{0}, {0}, {0}, {0}, {0}, {0}, {0}, {0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::atomic<uint64_t>& d = done[variant];
@@ -826,6 +862,13 @@ bool set_pair_smem_attribute(int variant) {
     return false;
   d.fetch_or(1ull << dev);
   return true;
+}
+
+template <bool kQ, bool kNT>
+cudaError_t launch_pair(bool scaled, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const CUtensorMap& ta,
+                        const CUtensorMap& tb, const CUtensorMap& tc, const PairArgsT<kQ>& a) {
+  if (scaled) return launch_kernel(fp8_gemm_pair_scaled_kernel<kQ, kNT>, grid, block, smem, stream, 2u, ta, tb, tc, a);
+  return launch_kernel(fp8_gemm_pair_kernel<kEpiCols, kQ, kNT>, grid, block, smem, stream, 2u, ta, tb, tc, a);
 }
 
 }  // namespace
@@ -838,12 +881,12 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   // A scale per 128 rows; per-row A scales take the FP32 promotion (exact too).
   const bool scaled = p.pow2_scales && !p.sa_per_row;
   const bool requant = p.rq.q != nullptr;
-  const int variant = (scaled ? 1 : 0) + (requant ? 2 : 0);
+  const bool nt = !p.a_mn && !p.b_mn;
+  const int variant = (scaled ? 1 : 0) + (requant ? 2 : 0) + (nt ? 4 : 0);
   const PairKind kind = pair_kind(variant);
   PairArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
   args.ld_c = p.ld_c;
-  args.rq = p.rq;
   args.sa = p.sa;
   args.sa_per_row = p.sa_per_row ? 1 : 0;
   args.sb = p.sb;
@@ -934,8 +977,19 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
       return DG_ERR_CUDA;
   }
 
-  if (launch_kernel(kind.kernel, dim3(2 * pairs), dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args) !=
-      cudaSuccess) {
+  cudaError_t e;
+  const dim3 grid(2 * pairs), block(kind.threads);
+  if (requant) {
+    PairArgsQ qa;
+    static_cast<PairArgs&>(qa) = args;
+    qa.rq = p.rq;
+    e = nt ? launch_pair<true, true>(scaled, grid, block, smem, stream, ta, tb, tc, qa)
+           : launch_pair<true, false>(scaled, grid, block, smem, stream, ta, tb, tc, qa);
+  } else {
+    e = nt ? launch_pair<false, true>(scaled, grid, block, smem, stream, ta, tb, tc, args)
+           : launch_pair<false, false>(scaled, grid, block, smem, stream, ta, tb, tc, args);
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }

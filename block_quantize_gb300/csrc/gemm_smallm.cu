@@ -31,6 +31,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/dgfp8.h"
 #include "dg_device.cuh"
@@ -79,7 +80,6 @@ struct SCfg {
 
 struct SmallArgs {
   __nv_bfloat16* c;
-  RequantOut rq;      // E4M3 output (requantizing kernels)
   int sa_per_row;  // sa is [M][K/128] instead of [1][K/128]
   int64_t ld_c;
   const float* sa;
@@ -97,6 +97,15 @@ struct SmallArgs {
   uint32_t a_stage_bytes, a_box_bytes;
   uint64_t wait_limit_ns;
 };
+
+// Arguments of the requantizing kernels. A separate type: with the extra
+// fields in the common struct the bf16 kernel with 256-column tiles spilled
+// more registers and lost ~1 us per decode call (measured).
+struct SmallArgsQ : SmallArgs {
+  RequantOut rq;      // E4M3 output
+};
+template <bool kQ>
+using SmallArgsT = std::conditional_t<kQ, SmallArgsQ, SmallArgs>;
 
 // Eight consecutive outputs at column gcol as bf16 (a 16-byte store when all
 // eight are inside the matrix, else element by element up to N).
@@ -138,7 +147,7 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, int gcol, int N
 // parity's slot again only after the next tile's exchange, which comes after
 // this CTA's reads. Returns false if a wait failed.
 template <int BN>
-__device__ __forceinline__ bool requant_cluster_tile(const SmallArgs& args, const float* part, uint32_t rank,
+__device__ __forceinline__ bool requant_cluster_tile(const SmallArgsQ& args, const float* part, uint32_t rank,
                                                      int split, int nb, int col_lo, int groups8, int work, int ew,
                                                      int lane, uint32_t tile_seq, uint32_t* rq_pmax,
                                                      uint32_t* rq_xmax, uint64_t* rq_bar, uint64_t* consumed_bar,
@@ -245,7 +254,7 @@ __device__ __forceinline__ bool requant_cluster_tile(const SmallArgs& args, cons
 template <int BN, bool kQ>
 __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
     fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                           const __grid_constant__ CUtensorMap tmap_b, const SmallArgs args) {
+                           const __grid_constant__ CUtensorMap tmap_b, const SmallArgsT<kQ> args) {
   using C = SCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -258,13 +267,19 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   if (a_read_end > off) off = a_read_end;  // an MMA reads 128 A rows from its stage
   float* part = reinterpret_cast<float*>(smem + off);
   off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
-  off = (off + 15) & ~static_cast<size_t>(15);
   // Requantized output (kQ): the block-max exchange.
-  uint8_t* rq_xchg = smem + off;
-  uint32_t* rq_pmax = reinterpret_cast<uint32_t*>(rq_xchg + C::kRqXchg);  // [2][128][kNBlk]
-  uint32_t* rq_xmax = rq_pmax + C::kRqPmaxWords;                           // [2][kMaxSplit][128][kNBlk]
-  uint64_t* rq_bar = reinterpret_cast<uint64_t*>(rq_xmax + C::kRqXmaxWords);  // amax[2], lmax[2]
-  if constexpr (kQ) off += C::kRqBytes;
+  uint8_t* rq_xchg = nullptr;
+  uint32_t* rq_pmax = nullptr;  // [2][128][kNBlk]
+  uint32_t* rq_xmax = nullptr;  // [2][kMaxSplit][128][kNBlk]
+  uint64_t* rq_bar = nullptr;   // amax[2], lmax[2]
+  if constexpr (kQ) {
+    off = (off + 15) & ~static_cast<size_t>(15);
+    rq_xchg = smem + off;
+    rq_pmax = reinterpret_cast<uint32_t*>(rq_xchg + C::kRqXchg);
+    rq_xmax = rq_pmax + C::kRqPmaxWords;
+    rq_bar = reinterpret_cast<uint64_t*>(rq_xmax + C::kRqXmaxWords);
+    off += C::kRqBytes;
+  }
   off = (off + 7) & ~static_cast<size_t>(7);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off);
   uint64_t* full_bar = bars;
@@ -444,16 +459,18 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
       }
       if (!ok) break;
 
-      if (split == 1 && kQ) {
-        // No peers: the epilogue slices exchange their maxima in this CTA.
-        bool unused = false;
-        if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, lg * 32, args.M, args.N, colt, ew, lane,
-                                               tile_seq, rq_xchg, args.rq, nullptr, nullptr, unused, abort_flag,
-                                               status, limit)) {
-          ok = false;
-          break;
+      if constexpr (kQ) {
+        if (split == 1) {
+          // No peers: the epilogue slices exchange their maxima in this CTA.
+          bool unused = false;
+          if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, lg * 32, args.M, args.N, colt, ew, lane,
+                                                 tile_seq, rq_xchg, args.rq, nullptr, nullptr, unused, abort_flag,
+                                                 status, limit)) {
+            ok = false;
+            break;
+          }
+          continue;
         }
-        continue;
       }
       if (split == 1) {
         // No peers: round this thread's row segment to bf16 and store it.
@@ -700,8 +717,11 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
       return DG_ERR_CUDA;
   }
   args.idesc = SCfg<BN>::kIdesc | idesc_majors(p.a_mn, p.b_mn);
+  SmallArgsT<kQ> kargs;
+  static_cast<SmallArgs&>(kargs) = args;
+  if constexpr (kQ) kargs.rq = p.rq;
   if (launch_kernel(fp8_gemm_splitk_kernel<BN, kQ>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
-                    smem, stream, static_cast<unsigned>(args.split), ta, tb, args) != cudaSuccess) {
+                    smem, stream, static_cast<unsigned>(args.split), ta, tb, kargs) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }
@@ -755,7 +775,6 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
   const uint32_t a_rows = p.a_mn ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
   args.a_box_bytes = a_rows * kBK;
   args.a_stage_bytes = (args.a_box_bytes + 1023u) / 1024u * 1024u;
-  args.rq = p.rq;
   return p.rq.q ? plan_and_run<true>(p, stream, sms, args) : plan_and_run<false>(p, stream, sms, args);
 }
 
