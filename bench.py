@@ -196,6 +196,14 @@ def run_reference(args):
     return 0
 
 
+# DRAM bytes (read + write) per GEMM launch of the step, averaged over its four
+# shapes: one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, caches
+# flushed before each launch) of fp8_gemm_pair_kernel<64, 0, 1>, recorded in
+# profiles/launches_bench_llm_projections.md. Per shape: 32.7, 45.0, 229.9,
+# 84.4 MB. Measured again whenever that kernel changes.
+GEMM_DRAM_BYTES_PER_LAUNCH = (32660992 + 44989184 + 229877760 + 84436480) / 4
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -356,7 +364,8 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * len(shapes()) * args.steps,
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
-                         "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                         "traffic": GEMM_DRAM_BYTES_PER_LAUNCH,
                          "peak_source": f"{peak_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (fp8/bf16 nominal)"},
             "cpu_baseline": {"value": ops / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle",
