@@ -38,7 +38,7 @@ __all__ = [
     "dg_fp8_grouped_gemm_contiguous", "dg_get_device_status", "dg_selftest_wait_timeout",
     "dg_quantize_fp8_1x128", "dg_fp8_gemm_nt_1x128", "dg_fp8_grouped_gemm_contiguous_1x128",
     "dg_fp8_gemm_nt_requant", "dg_fp8_grouped_gemm_contiguous_requant", "dg_fp8_gemm",
-    "dg_fp8_k_grouped_gemm_tn", "DG_LAYOUT_NT", "DG_LAYOUT_TN", "DG_LAYOUT_NN", "DG_LAYOUT_TT",
+    "dg_fp8_k_grouped_gemm_tn", "dg_fp8_gemm_requant", "DG_LAYOUT_NT", "DG_LAYOUT_TN", "DG_LAYOUT_NN", "DG_LAYOUT_TT",
     "declared_functions",
 ]
 
@@ -117,6 +117,9 @@ def lib() -> ctypes.CDLL:
         L.dg_fp8_grouped_gemm_contiguous_requant.restype = i32
         L.dg_fp8_gemm.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i64, i64, i64, i32, i32, vp]
         L.dg_fp8_gemm.restype = i32
+        L.dg_fp8_gemm_requant.argtypes = [vp, i64, vp, i32, i32, vp, i64, vp, i32, vp, i64, vp,
+                                          i64, i64, i64, i32, i32, vp]
+        L.dg_fp8_gemm_requant.restype = i32
         L.dg_fp8_k_grouped_gemm_tn.argtypes = [vp, i64, vp, i64, vp, vp, i64, vp, i32, vp, i64, i64, i32, vp]
         L.dg_fp8_k_grouped_gemm_tn.restype = i32
         L.dg_get_device_status.argtypes = [vp]
@@ -350,6 +353,44 @@ def dg_fp8_gemm(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Ten
                            _stream(c))
     _check(st, "dg_fp8_gemm")
     return c
+
+
+def dg_fp8_gemm_requant(a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor, sb: torch.Tensor, m: int, n: int,
+                        layout="NT", scale_mode: int = DG_SCALE_FP32, out_block_rows: int = 1,
+                        out_scale_mode: int = DG_SCALE_FP32, a_scale_rows: int = BLOCK,
+                        cq: torch.Tensor | None = None, cs: torch.Tensor | None = None):
+    """op(A) . op(B) in layout NT, TN, NN or TT (as dg_fp8_gemm) with the FP32
+    result requantized to E4M3 in the epilogue; returns (cq uint8 [m, n], cs).
+    sa is [ceil(m/128), K/128], or [m, K/128] with a_scale_rows = 1."""
+    lay = _LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    if lay not in _LAYOUTS.values():
+        raise ValueError(f"unknown layout {layout}")
+    a_t = lay in (DG_LAYOUT_TN, DG_LAYOUT_TT)
+    b_n = lay in (DG_LAYOUT_TN, DG_LAYOUT_NN)
+    a, b = _u8(a), _u8(b)
+    _cuda(a, torch.uint8, "a")
+    _cuda(b, torch.uint8, "b")
+    _cuda(sa, torch.float32, "sa")
+    _cuda(sb, torch.float32, "sb")
+    k = a.shape[0] if a_t else a.shape[1]
+    if tuple(a.shape) != ((k, m) if a_t else (m, k)) or tuple(b.shape) != ((k, n) if b_n else (n, k)):
+        raise ValueError("a or b does not match the layout, m, n and K")
+    kb = k // BLOCK
+    if a_scale_rows not in (1, BLOCK):
+        raise ValueError("a_scale_rows must be 1 or 128")
+    sa_rows = m if a_scale_rows == 1 else (m + BLOCK - 1) // BLOCK
+    if tuple(sa.shape) != (sa_rows, kb) or tuple(sb.shape) != ((n + BLOCK - 1) // BLOCK, kb):
+        raise ValueError("scale shape mismatch")
+    if not (sa.is_contiguous() and sb.is_contiguous()):
+        raise ValueError("scales must be contiguous")
+    cq, qb, cs = _requant_out(cq, cs, m, n, out_block_rows, a.device)
+    st = lib().dg_fp8_gemm_requant(
+        ctypes.c_void_p(qb.data_ptr()), _ld(qb, "cq"), ctypes.c_void_p(cs.data_ptr()), int(out_block_rows),
+        int(out_scale_mode), ctypes.c_void_p(a.data_ptr()), _ld(a, "a"), ctypes.c_void_p(sa.data_ptr()),
+        int(a_scale_rows), ctypes.c_void_p(b.data_ptr()), _ld(b, "b"), ctypes.c_void_p(sb.data_ptr()),
+        m, n, k, lay, int(scale_mode), _stream(a))
+    _check(st, "dg_fp8_gemm_requant")
+    return cq, cs
 
 
 def dg_fp8_k_grouped_gemm_tn(c: torch.Tensor, a: torch.Tensor, b: torch.Tensor, sa: torch.Tensor,

@@ -353,6 +353,51 @@ DG_API int dg_fp8_gemm(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, co
   return dg::launch_gemm(p, st);
 }
 
+DG_API int dg_fp8_gemm_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_block_rows, int out_scale_mode,
+                               const uint8_t* a, int64_t ld_a, const float* sa, int a_scale_rows, const uint8_t* b,
+                               int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K, int layout,
+                               int scale_mode, void* stream) {
+  if (layout < DG_LAYOUT_NT || layout > DG_LAYOUT_TT) return DG_ERR_INVALID_ARG;
+  if (M > 0 && N > 0) {
+    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
+    if (v != DG_OK) return v;
+  } else if (out_block_rows != 1 && out_block_rows != 128) {
+    return DG_ERR_INVALID_ARG;
+  }
+  const bool a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
+  const bool b_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_NN;
+  const int v = validate_gemm_rows(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, a_mn ? M : K,
+                                   b_mn ? N : K);
+  if (v == kEmpty) return DG_OK;
+  if (v != DG_OK) return v;
+  const int dev_st = check_device();
+  if (dev_st != DG_OK) return dev_st;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dg::RequantOut rq = make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N);
+  if (K == 0) return zero_requant_output(rq, M, N, st);
+  dg::GemmProblem p{};
+  p.rq = rq;
+  p.c = cq;
+  p.ld_c = ld_cq;
+  p.a = a;
+  p.ld_a = ld_a;
+  p.sa = sa;
+  p.b = b;
+  p.ld_b = ld_b;
+  p.sb = sb;
+  p.num_groups = 1;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_sms_cap = g_num_sms_cap.load();
+  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+  p.sa_per_row = a_scale_rows == 1;
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.ld_sa = p.ld_sb = K / 128;
+  return dg::launch_gemm(p, st);
+}
+
 DG_API int dg_fp8_k_grouped_gemm_tn(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                                     const uint8_t* b, int64_t ld_b, const float* sb, int num_groups,
                                     const int64_t* k_sizes, int64_t M, int64_t N, int scale_mode,

@@ -53,7 +53,7 @@ extern "C" {
 #define DG_API __attribute__((visibility("default")))
 #endif
 
-#define DG_ABI_VERSION 4u
+#define DG_ABI_VERSION 5u
 
 typedef enum {
     DG_OK = 0,
@@ -249,6 +249,18 @@ DG_API int dg_fp8_gemm(void *c, int64_t ld_c,
                        const uint8_t *b, int64_t ld_b, const float *sb,
                        int64_t M, int64_t N, int64_t K,
                        int layout, int scale_mode, void *stream);
+
+/* Dense GEMM in any layout with the output requantized in the epilogue: the
+ * layouts, strides and scales of dg_fp8_gemm, the output arguments
+ * (cq, ld_cq, cs, out_block_rows, out_scale_mode) and a_scale_rows of
+ * dg_fp8_gemm_nt_requant, which equals this call with layout DG_LAYOUT_NT.
+ * Row-wise A scales (a_scale_rows = 1) are [M][K/128] in every layout. */
+DG_API int dg_fp8_gemm_requant(uint8_t *cq, int64_t ld_cq, float *cs, int out_block_rows,
+                               int out_scale_mode,
+                               const uint8_t *a, int64_t ld_a, const float *sa, int a_scale_rows,
+                               const uint8_t *b, int64_t ld_b, const float *sb,
+                               int64_t M, int64_t N, int64_t K,
+                               int layout, int scale_mode, void *stream);
 
 /* K-grouped GEMM in the TN layout (pzsr.cn page §3.2: grouping along K, the
  * shape of MoE weight gradients): the K extent is cut into num_groups

@@ -25,7 +25,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_strings_alignment(L):
-    assert bq.dg_get_abi_version() == 4
+    assert bq.dg_get_abi_version() == 5
     assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
     for s in range(7):
         assert bq.dg_status_string(s)
@@ -186,6 +186,24 @@ def gemm_lay(L, **kw):
                          a["k"], a["layout"], a["mode"], None)
 
 
+def rq_lay(L, **kw):
+    a = dict(q=P, ldq=256, s=P, br=1, omode=0, a=P, lda=512, sa=P, arows=128, b=P, ldb=512, sb=P,
+             m=128, n=256, k=512, layout=0, mode=0)
+    a.update(kw)
+    return L.dg_fp8_gemm_requant(a["q"], a["ldq"], a["s"], a["br"], a["omode"], a["a"], a["lda"], a["sa"],
+                                 a["arows"], a["b"], a["ldb"], a["sb"], a["m"], a["n"], a["k"], a["layout"],
+                                 a["mode"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(layout=5), bq.DG_ERR_INVALID_ARG), (dict(br=7), bq.DG_ERR_INVALID_ARG),
+    (dict(layout=1, lda=112), bq.DG_ERR_INVALID_ARG), (dict(layout=2, ldb=240), bq.DG_ERR_INVALID_ARG),
+    (dict(layout=3, ldq=264), bq.DG_ERR_MISALIGNED), (dict(layout=1, m=0), bq.DG_OK),
+])
+def test_requant_layout_argument_errors(L, kw, status):
+    assert rq_lay(L, **kw) == status
+
+
 def kgrouped(L, sizes=(256, 128), **kw):
     a = dict(c=P, ldc=256, a=P, lda=128, sa=P, b=P, ldb=256, sb=P, m=128, n=256, mode=0)
     a.update(kw)
@@ -232,6 +250,8 @@ def test_valid_arguments_without_gpu_report_no_device(L):
     for layout in range(4):
         assert gemm_lay(L, layout=layout) == bq.DG_ERR_NO_DEVICE
     assert kgrouped(L) == bq.DG_ERR_NO_DEVICE
+    for layout in range(4):
+        assert rq_lay(L, layout=layout) == bq.DG_ERR_NO_DEVICE
     assert L.dg_selftest_wait_timeout(1000, None) == bq.DG_ERR_NO_DEVICE
 
 

@@ -235,3 +235,45 @@ def test_k_zero_writes_zero_codes_and_unit_scales():
     bq.dg_fp8_gemm_nt_requant(a, b, sa, sb, cq=cq, cs=cs)
     assert bq.dg_get_device_status() == bq.DG_OK
     assert torch.all(cq == 0) and torch.all(cs == 1.0)
+
+
+def _stored_padded(x, dev):
+    """x on the device with its row stride rounded up to 16 bytes (the TMA rule)."""
+    rows, cols = x.shape
+    buf = torch.zeros((rows, -(-cols // 16) * 16), dtype=torch.uint8, device=dev)
+    buf[:, :cols] = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+    return buf[:, :cols]
+
+
+@pytest.mark.parametrize("in_mode", [0, 1])
+@pytest.mark.parametrize("layout", ["TN", "NN", "TT"])
+@pytest.mark.parametrize("shape", [(300, 200, 1024), (16, 2304, 8192), (100, 300, 640)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_exact_layouts(oracle_mod, shape, layout, in_mode):
+    """Requantized output with MN-major operands: pair kernels (M > 128) and
+    the split-K kernel (M <= 128), per-row output scales."""
+    m, n, k = shape
+    qa, sa, qb, sb = _exact_operands(m, n, k, seed=3 * m + n)
+    dev = device()
+    a_st = qa.T if layout[0] == "T" else qa
+    b_st = qb.T if layout[1] == "N" else qb
+    cq, cs = bq.dg_fp8_gemm_requant(_stored_padded(a_st, dev), _stored_padded(b_st, dev), to_dev(sa, dev),
+                                    to_dev(sb, dev), m, n, layout, in_mode, 1, 0)
+    assert bq.dg_get_device_status() == bq.DG_OK
+    qr, sr, _, _ = oracle_mod.gemm_nt_requant(qa, sa, qb, sb, 1, 0)
+    assert np.array_equal(host(cs), sr) and np.array_equal(host(cq), qr)
+
+
+@pytest.mark.parametrize("layout", ["NT", "TT"])
+def test_exact_layouts_rowwise_a_scales_block_output(oracle_mod, layout):
+    """Per-row A scales in, 128 x 128 output blocks out, A stored either way
+    (B stays [N][K]: NT and TT)."""
+    m, n, k = 260, 384, 512
+    qa, sa, qb, sb = _exact_operands(m, n, k, seed=77, a_rows=1)
+    dev = device()
+    a_st = qa.T if layout[0] == "T" else qa
+    cq, cs = bq.dg_fp8_gemm_requant(_stored_padded(a_st, dev), to_dev(qb, dev), to_dev(sa, dev), to_dev(sb, dev),
+                                    m, n, layout, 0, 128, 0, a_scale_rows=1)
+    assert bq.dg_get_device_status() == bq.DG_OK
+    qr, sr, _, _ = oracle_mod.gemm_nt_requant(qa, sa, qb, sb, 128, 0, a_1x128=True)
+    assert np.array_equal(host(cs), sr) and np.array_equal(host(cq), qr)
