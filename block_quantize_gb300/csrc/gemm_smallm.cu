@@ -30,7 +30,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <type_traits>
 
 #include "../../include/dgfp8.h"
@@ -569,39 +571,39 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   cluster_sync_all();  // no CTA leaves while a peer may still read its partial
 }
 
-// Largest number of co-resident clusters of `split` CTAs for this kernel
-// (cached per device and split; the shared memory of one BN/kQ pair is fixed
-// by M, so the first query per shape class stands for the others).
+// Largest number of co-resident clusters of `split` CTAs for this kernel with
+// `smem` bytes of shared memory per CTA. The answer depends on the shared
+// memory, which follows M, so it is cached per (device, split, smem): decode
+// calls with varying M query the runtime once per distinct size.
 template <int BN, bool kQ>
 int max_active_clusters(int split, size_t smem) {
   static std::mutex mu;
-  static int cache[64][kMaxSplit + 1] = {};
-  static size_t cached_smem[64][kMaxSplit + 1] = {};
+  static std::map<std::tuple<int, int, size_t>, int> cache;
   if (split < 1 || split > kMaxSplit) return 0;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (cache[dev][split] == 0 || cached_smem[dev][split] != smem) {
-    cached_smem[dev][split] = smem;
-    cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(split * 256, 1, 1);
-    cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ>, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = -1;
-    }
-    cache[dev][split] = n;
+  const auto key = std::make_tuple(dev, split, smem);
+  const auto hit = cache.find(key);
+  if (hit != cache.end()) return hit->second;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(split * 256, 1, 1);
+  cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = -1;
   }
-  return cache[dev][split];
+  cache.emplace(key, n);
+  return n;
 }
 
 struct Plan {
