@@ -76,13 +76,6 @@ __device__ __forceinline__ uint8_t encode1(float v, float s, float r) {
   return static_cast<uint8_t>(c & 0xFFu);
 }
 
-// Runtime choice of the encoding mode for scale s.
-__device__ __forceinline__ uint32_t encode4_any(const float4 v, float s, float r, bool pow2) {
-  if (pow2) return encode4<1>(v, s, r);
-  if (s >= 0x1p-126f) return encode4<0>(v, s, r);
-  return encode4<2>(v, s, r);
-}
-
 // E4M3 codes of fl32(v / s) for four values held as two FP32 pairs (the
 // epilogue's accumulator layout), with the arithmetic of encode4 done in
 // packed f32x2 multiplies. r2 = (1/s, 1/s).
