@@ -55,18 +55,21 @@ template <int kMode>
 __device__ __forceinline__ uint32_t encode4(const float4 v, float s, float r) {
   if constexpr (kMode == 2) {
     return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
+  } else if constexpr (kMode == 1) {
+    return cvt2(v.x * r, v.y * r) | (cvt2(v.z * r, v.w * r) << 16);
   } else {
-    const float q0 = v.x * r, q1 = v.y * r, q2 = v.z * r, q3 = v.w * r;
-    const uint32_t c = cvt2(q0, q1) | (cvt2(q2, q3) << 16);
-    if constexpr (kMode == 1) {
-      return c;
-    } else {
-      constexpr float kLo = 1.0f - 0x1p-20f, kHi = 1.0f + 0x1p-20f;
-      const uint32_t lo = cvt2(q0 * kLo, q1 * kLo) | (cvt2(q2 * kLo, q3 * kLo) << 16);
-      const uint32_t hi = cvt2(q0 * kHi, q1 * kHi) | (cvt2(q2 * kHi, q3 * kHi) << 16);
-      if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
-      return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
-    }
+    // Products two at a time (mul.rn.f32x2: each lane rounded as a scalar multiply).
+    const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
+    const uint64_t q01 = fmul2(f32x2(__float_as_uint(v.x), __float_as_uint(v.y)), r2);
+    const uint64_t q23 = fmul2(f32x2(__float_as_uint(v.z), __float_as_uint(v.w)), r2);
+    const uint64_t lo2 = f32x2(__float_as_uint(1.0f - 0x1p-20f), __float_as_uint(1.0f - 0x1p-20f));
+    const uint64_t hi2 = f32x2(__float_as_uint(1.0f + 0x1p-20f), __float_as_uint(1.0f + 0x1p-20f));
+    const float2 la = f32x2_split(fmul2(q01, lo2)), lb = f32x2_split(fmul2(q23, lo2));
+    const float2 ha = f32x2_split(fmul2(q01, hi2)), hb = f32x2_split(fmul2(q23, hi2));
+    const uint32_t lo = cvt2(la.x, la.y) | (cvt2(lb.x, lb.y) << 16);
+    const uint32_t hi = cvt2(ha.x, ha.y) | (cvt2(hb.x, hb.y) << 16);
+    if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
+    return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
   }
 }
 
