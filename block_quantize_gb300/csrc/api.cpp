@@ -190,11 +190,21 @@ DG_API int dg_quantize_fp8_1x128(const void* x, int x_dtype, int64_t rows, int64
   return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
-// rq.q != nullptr: E4M3 output (c and ld_c then describe the codes).
+// Argument checks of a requantized output; with M or N zero only the block shape is checked.
+static int check_requant_args(const uint8_t* cq, int64_t ld_cq, const float* cs, int out_block_rows,
+                              int out_scale_mode, int a_scale_rows, int64_t M, int64_t N) {
+  if (M > 0 && N > 0) return validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
+  return (out_block_rows != 1 && out_block_rows != 128) ? DG_ERR_INVALID_ARG : DG_OK;
+}
+
+// One dense GEMM in any layout. rq.q != nullptr: E4M3 output (c and ld_c then describe the codes).
 static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                       const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
-                      int scale_mode, void* stream, bool a_1x128, const dg::RequantOut& rq) {
-  const int v = validate_gemm_common(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode);
+                      int layout, int scale_mode, void* stream, bool a_1x128, const dg::RequantOut& rq) {
+  const bool a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
+  const bool b_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_NN;
+  const int v = validate_gemm_rows(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, a_mn ? M : K,
+                                   b_mn ? N : K);
   if (v == kEmpty) return DG_OK;
   if (v != DG_OK) return v;
   const int dev_st = check_device();
@@ -219,6 +229,8 @@ static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, con
   p.num_sms_cap = g_num_sms_cap.load();
   p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
   p.sa_per_row = a_1x128;
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
   p.ld_sa = p.ld_sb = K / 128;
   return dg::launch_gemm(p, st);
 }
@@ -226,27 +238,25 @@ static int gemm_dense(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, con
 DG_API int dg_fp8_gemm_nt(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                           const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
                           int64_t K, int scale_mode, void* stream) {
-  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, false, dg::RequantOut{});
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, DG_LAYOUT_NT, scale_mode, stream, false,
+                    dg::RequantOut{});
 }
 
 DG_API int dg_fp8_gemm_nt_1x128(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
                                 const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
                                 int64_t K, int scale_mode, void* stream) {
-  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, true, dg::RequantOut{});
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, DG_LAYOUT_NT, scale_mode, stream, true,
+                    dg::RequantOut{});
 }
 
 DG_API int dg_fp8_gemm_nt_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_block_rows, int out_scale_mode,
                                   const uint8_t* a, int64_t ld_a, const float* sa, int a_scale_rows,
                                   const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N,
                                   int64_t K, int scale_mode, void* stream) {
-  if (M > 0 && N > 0) {
-    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
-    if (v != DG_OK) return v;
-  } else if (out_block_rows != 1 && out_block_rows != 128) {
-    return DG_ERR_INVALID_ARG;
-  }
-  return gemm_dense(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, stream, a_scale_rows == 1,
-                    make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
+  const int v = check_requant_args(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows, M, N);
+  if (v != DG_OK) return v;
+  return gemm_dense(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, DG_LAYOUT_NT, scale_mode, stream,
+                    a_scale_rows == 1, make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
 }
 
 static int gemm_grouped(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
@@ -308,12 +318,8 @@ DG_API int dg_fp8_grouped_gemm_contiguous_requant(uint8_t* cq, int64_t ld_cq, fl
                                                   const float* sb, int num_groups, const int32_t* m_indices,
                                                   int64_t M_tot, int64_t N, int64_t K, int scale_mode,
                                                   void* stream) {
-  if (M_tot > 0 && N > 0) {
-    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
-    if (v != DG_OK) return v;
-  } else if (out_block_rows != 1 && out_block_rows != 128) {
-    return DG_ERR_INVALID_ARG;
-  }
+  const int v = check_requant_args(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows, M_tot, N);
+  if (v != DG_OK) return v;
   return gemm_grouped(cq, ld_cq, a, ld_a, sa, b, sb, num_groups, m_indices, M_tot, N, K, scale_mode, stream,
                       a_scale_rows == 1, make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
 }
@@ -322,35 +328,8 @@ DG_API int dg_fp8_gemm(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, co
                        const uint8_t* b, int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K,
                        int layout, int scale_mode, void* stream) {
   if (layout < DG_LAYOUT_NT || layout > DG_LAYOUT_TT) return DG_ERR_INVALID_ARG;
-  const bool a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
-  const bool b_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_NN;
-  const int v = validate_gemm_rows(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, a_mn ? M : K,
-                                   b_mn ? N : K);
-  if (v == kEmpty) return DG_OK;
-  if (v != DG_OK) return v;
-  const int dev_st = check_device();
-  if (dev_st != DG_OK) return dev_st;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(c, ld_c, M, N, st);
-  dg::GemmProblem p{};
-  p.c = c;
-  p.ld_c = ld_c;
-  p.a = a;
-  p.ld_a = ld_a;
-  p.sa = sa;
-  p.b = b;
-  p.ld_b = ld_b;
-  p.sb = sb;
-  p.num_groups = 1;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.num_sms_cap = g_num_sms_cap.load();
-  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
-  p.a_mn = a_mn;
-  p.b_mn = b_mn;
-  p.ld_sa = p.ld_sb = K / 128;
-  return dg::launch_gemm(p, st);
+  return gemm_dense(c, ld_c, a, ld_a, sa, b, ld_b, sb, M, N, K, layout, scale_mode, stream, false,
+                    dg::RequantOut{});
 }
 
 DG_API int dg_fp8_gemm_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_block_rows, int out_scale_mode,
@@ -358,44 +337,10 @@ DG_API int dg_fp8_gemm_requant(uint8_t* cq, int64_t ld_cq, float* cs, int out_bl
                                int64_t ld_b, const float* sb, int64_t M, int64_t N, int64_t K, int layout,
                                int scale_mode, void* stream) {
   if (layout < DG_LAYOUT_NT || layout > DG_LAYOUT_TT) return DG_ERR_INVALID_ARG;
-  if (M > 0 && N > 0) {
-    const int v = validate_requant_out(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows);
-    if (v != DG_OK) return v;
-  } else if (out_block_rows != 1 && out_block_rows != 128) {
-    return DG_ERR_INVALID_ARG;
-  }
-  const bool a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
-  const bool b_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_NN;
-  const int v = validate_gemm_rows(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, scale_mode, a_mn ? M : K,
-                                   b_mn ? N : K);
-  if (v == kEmpty) return DG_OK;
+  const int v = check_requant_args(cq, ld_cq, cs, out_block_rows, out_scale_mode, a_scale_rows, M, N);
   if (v != DG_OK) return v;
-  const int dev_st = check_device();
-  if (dev_st != DG_OK) return dev_st;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const dg::RequantOut rq = make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N);
-  if (K == 0) return zero_requant_output(rq, M, N, st);
-  dg::GemmProblem p{};
-  p.rq = rq;
-  p.c = cq;
-  p.ld_c = ld_cq;
-  p.a = a;
-  p.ld_a = ld_a;
-  p.sa = sa;
-  p.b = b;
-  p.ld_b = ld_b;
-  p.sb = sb;
-  p.num_groups = 1;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.num_sms_cap = g_num_sms_cap.load();
-  p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
-  p.sa_per_row = a_scale_rows == 1;
-  p.a_mn = a_mn;
-  p.b_mn = b_mn;
-  p.ld_sa = p.ld_sb = K / 128;
-  return dg::launch_gemm(p, st);
+  return gemm_dense(cq, ld_cq, a, ld_a, sa, b, ld_b, sb, M, N, K, layout, scale_mode, stream,
+                    a_scale_rows == 1, make_requant(cq, ld_cq, cs, out_block_rows, out_scale_mode, N));
 }
 
 DG_API int dg_fp8_k_grouped_gemm_tn(void* c, int64_t ld_c, const uint8_t* a, int64_t ld_a, const float* sa,
