@@ -51,6 +51,23 @@ __device__ __forceinline__ uint32_t cvt2(float a, float b) {
 // included -- does too (rounding to E4M3 is monotone), so that code is exact.
 // Otherwise (an E4M3 rounding boundary within 2^-20 of q, about one value in
 // 2^15) the element is divided exactly.
+// kMode 0 without its fallback: the codes of q (1 - 2^-20), which are exact
+// when ok (no E4M3 rounding boundary near q); otherwise the caller divides.
+// Products two at a time (mul.rn.f32x2: each lane rounded as a scalar multiply).
+__device__ __forceinline__ uint32_t encode4_bracketed(const float4 v, float r, bool& ok) {
+  const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
+  const uint64_t q01 = fmul2(f32x2(__float_as_uint(v.x), __float_as_uint(v.y)), r2);
+  const uint64_t q23 = fmul2(f32x2(__float_as_uint(v.z), __float_as_uint(v.w)), r2);
+  const uint64_t lo2 = f32x2(__float_as_uint(1.0f - 0x1p-20f), __float_as_uint(1.0f - 0x1p-20f));
+  const uint64_t hi2 = f32x2(__float_as_uint(1.0f + 0x1p-20f), __float_as_uint(1.0f + 0x1p-20f));
+  const float2 la = f32x2_split(fmul2(q01, lo2)), lb = f32x2_split(fmul2(q23, lo2));
+  const float2 ha = f32x2_split(fmul2(q01, hi2)), hb = f32x2_split(fmul2(q23, hi2));
+  const uint32_t lo = cvt2(la.x, la.y) | (cvt2(lb.x, lb.y) << 16);
+  const uint32_t hi = cvt2(ha.x, ha.y) | (cvt2(hb.x, hb.y) << 16);
+  ok = lo == hi;
+  return lo;
+}
+
 template <int kMode>
 __device__ __forceinline__ uint32_t encode4(const float4 v, float s, float r) {
   if constexpr (kMode == 2) {
@@ -58,18 +75,32 @@ __device__ __forceinline__ uint32_t encode4(const float4 v, float s, float r) {
   } else if constexpr (kMode == 1) {
     return cvt2(v.x * r, v.y * r) | (cvt2(v.z * r, v.w * r) << 16);
   } else {
-    // Products two at a time (mul.rn.f32x2: each lane rounded as a scalar multiply).
-    const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
-    const uint64_t q01 = fmul2(f32x2(__float_as_uint(v.x), __float_as_uint(v.y)), r2);
-    const uint64_t q23 = fmul2(f32x2(__float_as_uint(v.z), __float_as_uint(v.w)), r2);
-    const uint64_t lo2 = f32x2(__float_as_uint(1.0f - 0x1p-20f), __float_as_uint(1.0f - 0x1p-20f));
-    const uint64_t hi2 = f32x2(__float_as_uint(1.0f + 0x1p-20f), __float_as_uint(1.0f + 0x1p-20f));
-    const float2 la = f32x2_split(fmul2(q01, lo2)), lb = f32x2_split(fmul2(q23, lo2));
-    const float2 ha = f32x2_split(fmul2(q01, hi2)), hb = f32x2_split(fmul2(q23, hi2));
-    const uint32_t lo = cvt2(la.x, la.y) | (cvt2(lb.x, lb.y) << 16);
-    const uint32_t hi = cvt2(ha.x, ha.y) | (cvt2(hb.x, hb.y) << 16);
-    if (lo == hi) return lo;  // no E4M3 rounding boundary near q: exact
-    return cvt2(v.x / s, v.y / s) | (cvt2(v.z / s, v.w / s) << 16);
+    bool ok;
+    const uint32_t c = encode4_bracketed(v, r, ok);
+    return ok ? c : encode4<2>(v, s, r);
+  }
+}
+
+// encode4 over n groups at once: every group's codes are formed before any
+// fallback division, so the groups' independent work can interleave.
+template <int kMode, int n>
+__device__ __forceinline__ void encode4_n(const float4 (&v)[n], uint32_t (&code)[n], float s, float r) {
+  if constexpr (kMode == 0) {
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      bool ok;
+      code[i] = encode4_bracketed(v[i], r, ok);
+      bad |= (ok ? 0u : 1u) << i;
+    }
+    if (bad != 0u) {
+#pragma unroll
+      for (int i = 0; i < n; ++i)
+        if ((bad >> i) & 1u) code[i] = encode4<2>(v[i], s, r);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < n; ++i) code[i] = encode4<kMode>(v[i], s, r);
   }
 }
 

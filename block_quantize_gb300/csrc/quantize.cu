@@ -65,6 +65,14 @@ __device__ __forceinline__ void encode_store(const float4 (&v)[kRowsPerWarp], in
                                              int64_t rows, int64_t cols, uint8_t* __restrict__ q,
                                              int64_t ld_q, float s, float r) {
   const bool full4 = c0 + 3 < cols;
+  if (kVec && full4 && r0 + kRowsPerWarp <= rows) {  // all of this thread's groups are inside
+    uint32_t code[kRowsPerWarp];
+    encode4_n<kMode>(v, code, s, r);
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+      __stcs(reinterpret_cast<unsigned int*>(q + (r0 + i) * ld_q + c0), code[i]);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < kRowsPerWarp; ++i) {
     const int64_t row = r0 + i;
@@ -336,27 +344,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kPow2) my_s = pow2_round_up(my_s);
       const float my_r = 1.0f / my_s;
       if (lane < kRowsPerWarp && r0 + lane < rows) scales[(r0 + lane) * blocks_per_row + bj] = my_s;
+      // Every row's codes first (independent work that can interleave), then
+      // the rare exact divisions, then the stores.
+      uint32_t code[kRowsPerWarp];
+      float s_row[kRowsPerWarp];
+      uint32_t bad = 0;
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i) {
         const float s = __shfl_sync(0xFFFFFFFFu, my_s, i);
+        const float r = __shfl_sync(0xFFFFFFFFu, my_r, i);
+        s_row[i] = s;
+        if constexpr (kPow2) {
+          code[i] = encode4<1>(v[i], s, r);
+        } else {
+          bool ok;
+          code[i] = encode4_bracketed(v[i], r, ok);
+          bad |= (ok && s >= 0x1p-126f ? 0u : 1u) << i;  // a subnormal scale is always divided
+        }
+      }
+      if (!kPow2 && bad != 0u) {
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i)
+          if ((bad >> i) & 1u) code[i] = encode4<2>(v[i], s_row[i], 0.0f);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowsPerWarp; ++i) {
         const int64_t row = r0 + i;
         if (row < rows) {
-          const float r = __shfl_sync(0xFFFFFFFFu, my_r, i);
-          uint32_t code;
-          if constexpr (kPow2) {
-            code = encode4<1>(v[i], s, r);
-          } else if (s >= 0x1p-126f) {
-            code = encode4<0>(v[i], s, r);
-          } else {
-            code = encode4<2>(v[i], s, r);
-          }
           uint8_t* out = q + row * ld_q + c0;
           if (c0 + 3 < cols) {
-            __stcs(reinterpret_cast<unsigned int*>(out), code);
+            __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
           } else {
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              if (c0 + t < cols) out[t] = static_cast<uint8_t>((code >> (8 * t)) & 0xFFu);
+              if (c0 + t < cols) out[t] = static_cast<uint8_t>((code[i] >> (8 * t)) & 0xFFu);
           }
         }
       }
