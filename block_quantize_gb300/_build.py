@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdgfp8.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cpp", "quantize.cu", "gemm.cu", "gemm_smallm.cu", "gemm_pair.cu"]
+SOURCES = ["api.cpp", "quantize.cu", "gemm.cu", "gemm_smallm.cu", "gemm_pair.cu", "gemv.cu"]
 HEADERS = ["dg_device.cuh", "dg_encode.cuh", "dg_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

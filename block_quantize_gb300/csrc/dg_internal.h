@@ -97,6 +97,11 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream);
 bool small_m_supported(int64_t M, const void* m_indices);
 int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream);
 
+// M = 1 with K-major B and bf16 output, all SMs allowed: the streaming kernel
+// of gemv.cu.
+bool gemv_supported(const GemmProblem& p);
+int launch_gemv(const GemmProblem& p, cudaStream_t stream);
+
 // Reads and clears the current device's status word (a bitmask of kernel
 // timeouts). Returns the CUDA error of the copy.
 cudaError_t read_and_clear_status(unsigned int* out);

@@ -816,7 +816,8 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DG_ERR_NO_DEVICE;
   const int sms = device_info(dev).num_sms;
   if (sms <= 0) return DG_ERR_NO_DEVICE;
-  // Decode shapes (M <= 128): cluster split-K.
+  // Decode shapes: one row streams B (gemv.cu); M <= 128, cluster split-K.
+  if (!block_n_override() && gemv_supported(p)) return launch_gemv(p, stream);
   if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
   if (!block_n_override() && p.m_indices == nullptr && p.M > kBM) {
     const int r = launch_gemm_pair(p, stream);

@@ -276,6 +276,20 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_c);
+    // The first stages' B half-tiles of this CTA's first tile start streaming
+    // into L2 while the preceding grid finishes.
+    if (pair < args.num_pm * args.num_nb) {
+      int pm, nb;
+      pair_tile_coords(pair, args.num_pm, args.num_nb, pm, nb);
+      const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
+      const int n_pre = min(S, args.num_kb);
+      for (int kb = 0; kb < n_pre; ++kb) {
+        if (!kNT && args.b_mn)
+          tma_prefetch_2d(&tmap_b, brow, kb * kBK);
+        else
+          tma_prefetch_2d(&tmap_b, kb * kBK, brow);
+      }
+    }
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kNumBuf * kBN);
   tc_fence_before();

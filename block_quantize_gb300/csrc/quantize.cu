@@ -283,6 +283,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // The first stages' blocks start streaming into L2 while the preceding grid finishes.
+    for (int j = 0; j < kStages; ++j) {
+      const int64_t blk = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
+      if (blk >= nblocks) break;
+      const int64_t bi = blk / blocks_per_row, bj = blk - bi * blocks_per_row;
+      tma_prefetch_2d(&tmap_x, static_cast<int32_t>(bj * kBlock), static_cast<int32_t>(bi * kBlock));
+    }
   }
   __syncthreads();
   pdl_wait();
