@@ -8,12 +8,13 @@
 // does two FLOPs per byte, so the HBM stream alone sets its time. Tensor-core
 // tiles would only add what a split-K schedule costs at this size: 128-byte
 // TMA rows, whole waves of tiles and a reduction between CTAs. Instead:
-//   * a CTA owns kRows = 8 consecutive rows of B (8 outputs), all in one
-//     128-row scale block, and adds nothing across CTAs;
+//   * a CTA owns kRows consecutive rows of B (kRows outputs), all in one
+//     128-row scale block, and adds nothing across CTAs. kRows is 4 for
+//     K <= 4096 and 8 above (measured: more, smaller CTAs suit short rows);
 //   * thread t owns the 16-byte K segments t, t + T, t + 2T, ... of those rows
 //     (T threads). It loads the segment's 16 A values once, multiplies them by
-//     the segment's K-block factor, then reads the segment in each of the 8 B
-//     rows and accumulates 16 products per row with FP32 FMAs. Lanes read
+//     the segment's K-block factor, then reads the segment in each of the
+//     kRows B rows and accumulates 16 products per row with FP32 FMAs. Lanes read
 //     consecutive segments, so every warp load is 512 contiguous bytes;
 //   * the CTA adds its threads' sums in a fixed order (warp shuffles, then
 //     shared memory) and rounds them to bf16.
@@ -36,7 +37,6 @@
 namespace dg {
 namespace {
 
-constexpr int kRows = 8;          // rows of B (outputs) per CTA; divides 128
 constexpr int kMaxThreads = 256;  // 16-byte K segments in flight per row per CTA
 
 struct GemvArgs {
@@ -70,7 +70,9 @@ __device__ __forceinline__ void decode16(const uint4 v, float (&x)[16]) {
   }
 }
 
-__global__ void __launch_bounds__(kMaxThreads, 3) fp8_gemv_kernel(const GemvArgs args) {
+// kRows rows of B (outputs) per CTA; divides 128.
+template <int kRows>
+__global__ void __launch_bounds__(kMaxThreads, kRows <= 4 ? 4 : 3) fp8_gemv_kernel(const GemvArgs args) {
   __shared__ float red[kMaxThreads / 32][kRows];
   const int T = static_cast<int>(blockDim.x);  // a multiple of 32
   const int t = static_cast<int>(threadIdx.x);
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kMaxThreads, 3) fp8_gemv_kernel(const GemvArgs
   for (int j = 0; j < kRows; ++j) acc[j] = 0.f;
 
   for (int u = t; u < args.segs; u += T) {
-    // The B segment of every row first (8 loads in flight), then A and the factor.
+    // The B segment of every row first (kRows loads in flight), then A and the factor.
     uint4 bv[kRows];
 #pragma unroll
     for (int j = 0; j < kRows; ++j)
@@ -155,9 +157,13 @@ int launch_gemv(const GemmProblem& p, cudaStream_t stream) {
   args.N = p.N;
   args.segs = static_cast<int>(p.K / 16);
   const int threads = std::min(kMaxThreads, (args.segs + 31) / 32 * 32);
-  const int64_t grid = (p.N + kRows - 1) / kRows;
-  if (launch_kernel(fp8_gemv_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, stream, 0, args) !=
-      cudaSuccess) {
+  const bool short_k = p.K <= 4096;
+  const int rows = short_k ? 4 : 8;
+  const int64_t grid = (p.N + rows - 1) / rows;
+  const cudaError_t e =
+      short_k ? launch_kernel(fp8_gemv_kernel<4>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, stream, 0, args)
+              : launch_kernel(fp8_gemv_kernel<8>, dim3(static_cast<unsigned>(grid)), dim3(threads), 0, stream, 0, args);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }

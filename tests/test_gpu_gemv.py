@@ -7,8 +7,9 @@ walkthrough §2.2, §3.2; pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析"
   the split-K kernel's (the kernel single rows take while an SM cap is set).
 * General cases: |C_gpu - C_ref| <= 8e-3 |C_ref| + 1e-4 sum_k |a~ b~|, on the
   decode shapes 1 x 24576 x 1536 and 1 x 7168 x 16384 among others.
-* Ragged N (not a multiple of the kernel's 8 rows), K not a multiple of 512
-  (partial warps) or of 4096 (partial last pass of the CTA), padded row strides."""
+* Ragged N (not a multiple of the kernel's 4 or 8 rows per CTA), K not a
+  multiple of 512 (partial warps) or of 4096 (partial last pass of the CTA),
+  padded row strides."""
 import numpy as np
 import pytest
 import torch
