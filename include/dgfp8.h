@@ -103,7 +103,9 @@ DG_API int dg_get_mk_alignment_for_contiguous_layout(void);
 
 /* Cap the number of SMs the GEMM's persistent grid uses (0 = all SMs), the
  * DG_SET_NUM_SMS knob of pzsr.cn page §3.3. Applies to later calls from every
- * thread. Returns DG_ERR_INVALID_ARG for n < 0. */
+ * thread. Single-row GEMMs (M = 1) stream B over every SM when no cap is set
+ * and run on the capped persistent kernels when one is. Returns
+ * DG_ERR_INVALID_ARG for n < 0. */
 DG_API int dg_set_num_sms(int n);
 
 /* The current cap (0 = all SMs). */
