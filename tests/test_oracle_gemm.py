@@ -174,3 +174,42 @@ def test_grouped_rejects_bad_expert_id(oracle_mod):
     mi[3] = 2
     with pytest.raises(ValueError):
         oracle_mod.grouped_gemm_contiguous(qa, sa, qb, sb, mi)
+
+
+def _fp32_single_row(qa, sa, qb, sb, factor_first):
+    """One row of A against B in FP32 arithmetic, summed in K order: either the
+    K block's partial sum P_kb is formed first and then scaled, acc += s (sum a b),
+    or each A value is scaled first, acc += (s a) b. Both are FP32 evaluations of
+    the method's sum (walkthrough §2.2: the product block carries sa * sb)."""
+    f32 = np.float32
+    a = _decode(qa).astype(f32)[0]
+    b = _decode(qb).astype(f32)
+    n, k = b.shape
+    acc = np.zeros(n, f32)
+    for kb in range(k // 128):
+        s = (sa[0, kb].astype(f32) * sb[np.arange(n) // 128, kb].astype(f32)).astype(f32)
+        ks = slice(128 * kb, 128 * kb + 128)
+        if factor_first:
+            for kk in range(ks.start, ks.stop):
+                acc = (acc + ((s * a[kk]).astype(f32) * b[:, kk]).astype(f32)).astype(f32)
+        else:
+            p = np.zeros(n, f32)
+            for kk in range(ks.start, ks.stop):
+                p = (p + (a[kk] * b[:, kk]).astype(f32)).astype(f32)
+            acc = (acc + (s * p).astype(f32)).astype(f32)
+    return acc.astype(np.float64)
+
+
+@pytest.mark.parametrize("factor_first", [False, True])
+def test_fp32_factor_order_within_parity_bound(oracle_mod, factor_first):
+    """Whether the factor sa * sb multiplies the K block's FP32 partial sum or
+    each A value before the FP32 sum, the result stays within the parity bound
+    8e-3 |C| + 1e-4 sum|a~ b~| of the exact (float64) oracle result, with a
+    margin: the bound the GPU kernels are held to covers either order."""
+    n, k = 300, 2048
+    qa, sa = oracle_mod.quantize(synthetic.lognormal_rows((1, k), 77), 0)
+    qb, sb = oracle_mod.quantize(synthetic.lognormal_rows((n, k), 78), 0)
+    ref, mag = oracle_mod.gemm_nt(qa, sa, qb, sb)
+    got = _fp32_single_row(qa, sa, qb, sb, factor_first)
+    bound = 8e-3 * np.abs(ref[0]) + 1e-4 * mag[0]
+    assert np.all(np.abs(got - ref[0]) <= 0.1 * bound)
