@@ -17,9 +17,20 @@ e2e     = the same metric through the same C-ABI calls with host buffers: the
           FP32 activations are copied from pinned host memory and C is copied
           back every step, inside the timed region.
 roofline = the GEMM kernel (the dominant one), per launch: 2 M N K / its mean
-          CUDA-event duration over K further steps with events around every
-          GEMM launch, against the FP8 dense peak (measured bf16 cuBLAS peak
-          x 2, the nominal fp8/bf16 ratio).
+          CUDA-event duration over about one second of further steps with
+          events around every GEMM launch, against the FP8 dense peak (measured
+          bf16 cuBLAS burst peak x 2, the nominal fp8/bf16 ratio; the kernel
+          runs at the full SM clock, which the clock samples of that region
+          show, so the burst figure measured at that clock is the one that
+          applies).
+configs = the other workloads of the metric, each timed in a bounded region
+          after the line's own: the quantizer on a 16384x7168 FP32 activation
+          (GB/s), the decode GEMMs M in {1,16,64,128} x (N,K) in
+          {(24576,1536),(7168,16384)} (GB/s, graph-replayed), the MoE grouped
+          GEMM of 8 experts (TFLOP/s) and the squares 4096^3 and 8192^3 with
+          FP32 and power-of-two scales (TFLOP/s), each with its fraction of the
+          roofline that bounds it. Memory-bound cases rotate input copies
+          beyond L2.
 
 --impl reference times the CPU oracle (the only reference this path has) on a
 bounded sample of the same workload: the first 128 rows of every activation
@@ -260,10 +271,9 @@ def run_ours(args):
     # Device-timed regions. (1) `value`: K steps back to back, nothing between
     # the launches, so each kernel's prologue overlaps the previous kernel's
     # tail (programmatic dependent launch); an event recorded between two
-    # launches would serialize them. (2) `roofline`: K more steps with every
-    # GEMM launch bracketed by events on the launching stream.
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in shapes()] for _ in range(args.steps)]
+    # launches would serialize them. (2) `roofline`: about one second of further
+    # steps (at least K) with every GEMM launch bracketed by events on the
+    # launching stream, long enough for the clock sampler to see it.
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local) if rank == 0 else None
@@ -278,17 +288,23 @@ def run_ours(args):
     t1.record(stream)
     barrier()
     w1 = time.time()
+    ms = t0.elapsed_time(t1)
+    roof_steps = max(args.steps, int(1000.0 / max(ms / args.steps, 1e-3)))
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in shapes()] for _ in range(roof_steps)]
+    w1 = time.time()
     r0.record(stream)
-    for s in range(args.steps):
+    for s in range(roof_steps):
         step(ev[s])
     r1.record(stream)
     barrier()
     w2 = time.time()
     clock_info = clocks.stop((w0, w2)) if clocks else None
-    ms = t0.elapsed_time(t1)
+    if clock_info is not None:
+        clock_info["roofline_region_s"] = w2 - w1
     ms_with_events = r0.elapsed_time(r1)
     gemm_ms = [[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(len(shapes()))]
-               for s in range(args.steps)]
+               for s in range(roof_steps)]
     status = bq.dg_get_device_status()
     if status != bq.DG_OK:
         raise RuntimeError(f"kernel status {bq.dg_status_string(status)}")
@@ -356,15 +372,17 @@ def run_ours(args):
         value = world * flops * args.steps / (ms * 1e-3) / 1e12
         e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
         peaks, peak_src = measured_peaks()
-        fp8_peak = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+        fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+        fp8_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
         per_shape = []
         tot_flops, tot_ms = 0.0, 0.0
         for i, (m, n, k) in enumerate(shapes()):
-            t = statistics.mean(gemm_ms[s][i] for s in range(args.steps))
+            t = statistics.mean(gemm_ms[s][i] for s in range(roof_steps))
             per_shape.append({"M": m, "N": n, "K": k, "ms": t, "tflops": 2.0 * m * n * k / (t * 1e-3) / 1e12})
             tot_flops += 2.0 * m * n * k
             tot_ms += t
         gemm_tflops = tot_flops / (tot_ms * 1e-3) / 1e12
+        configs = config_records(dev, gen, stream, fp8_peak, peaks["hbm_gbs"]) if args.configs else None
         ops, secs, cores = cpu_sample(256, reps=3)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -379,16 +397,20 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                          "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                          "traffic": GEMM_DRAM_BYTES_PER_LAUNCH,
-                         "peak_source": f"{peak_src} bf16_tflops_sustained x {FP8_PER_BF16:g} (fp8/bf16 nominal)",
-                         "timed": f"{args.steps} steps after the `value` region, events around each GEMM launch"},
+                         "peak_source": f"{peak_src} bf16_tflops (burst) x {FP8_PER_BF16:g} (fp8/bf16 nominal)",
+                         "peak_sustained": fp8_sustained, "frac_of_sustained": gemm_tflops / fp8_sustained,
+                         "timed": f"{roof_steps} steps (~1 s) after the `value` region, events around each "
+                                  "GEMM launch"},
             "cpu_baseline": {"value": ops / secs / 1e12, "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle",
                              "sample": "first 256 rows of each of the 4 activations, quantize + GEMM, 3 reps"},
             "clocks": clock_info,
             "kernels": {"gemm_per_shape": per_shape,
-                        "ms_per_step_with_events": ms_with_events / args.steps,
-                        "quantize_ms_per_step": ms_with_events / args.steps - tot_ms},
+                        "ms_per_step_with_events": ms_with_events / roof_steps,
+                        "quantize_ms_per_step": ms_with_events / roof_steps - tot_ms},
         }
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -458,6 +480,131 @@ def _rand_fp8(shape, dev, gen, mode):
     return bq.dg_quantize_fp8_block(x, mode)
 
 
+def _gemm_bytes(m, n, k):
+    """Algorithmic bytes of one dense GEMM: A and B codes, their scales, C in bf16."""
+    return m * k + n * k + 2 * m * n + 4 * (-(-m // 128) + -(-n // 128)) * (k // 128)
+
+
+def gemm_records(dev, gen, stream, dims, mode, steps, warmup, fp8_peak):
+    """Dense GEMMs (M, N, K) with B copies rotated beyond L2: TFLOP/s and the
+    fraction of the FP8 burst peak."""
+    import torch
+    import block_quantize_gb300 as bq
+    res = []
+    for (m, n, k) in dims:
+        qa, sa = _rand_fp8((m, k), dev, gen, mode)
+        copies = max(1, min(8, -(-3 * L2_BYTES // (n * k))))
+        bs = [_rand_fp8((n, k), dev, gen, mode) for _ in range(copies)]
+        c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb, mode) for qb, sb in bs]
+        ms = statistics.median(_time_each(stream, fns, steps, warmup))
+        _check_status(bq, f"GEMM {m}x{n}x{k}")
+        tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+        res.append({"M": m, "N": n, "K": k, "scales": "ue8m0" if mode else "fp32", "us": ms * 1e3,
+                    "tflops": tf, "bound": "tensor", "frac": tf / fp8_peak,
+                    "gbs": _gemm_bytes(m, n, k) / (ms * 1e-3) / 1e9})
+        del bs, qa, sa, c
+    return res
+
+
+def small_records(dev, gen, stream, steps, warmup, hbm, ms_=None):
+    """Decode GEMMs (M <= 128): HBM-bound, so GB/s of algorithmic bytes against
+    the measured copy bandwidth; launches of a few microseconds are replayed
+    back to back from a CUDA graph (B copies rotated beyond L2)."""
+    import torch
+    import block_quantize_gb300 as bq
+    res = []
+    for n, k in synthetic.SMALL_NK:
+        copies = max(1, -(-3 * L2_BYTES // (n * k)))
+        bs = [_rand_fp8((n, k), dev, gen, 0) for _ in range(copies)]
+        for m in (ms_ or synthetic.SMALL_M):
+            qa, sa = _rand_fp8((m, k), dev, gen, 0)
+            c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb) for qb, sb in bs]
+            ms_event = statistics.median(_time_each(stream, fns, steps, warmup))
+            ms = _time_graph(stream, fns * max(1, 24 // len(fns)), max(steps, 10))
+            _check_status(bq, f"GEMM {m}x{n}x{k}")
+            byts = _gemm_bytes(m, n, k)
+            res.append({"M": m, "N": n, "K": k, "us": ms * 1e3, "us_single_launch": ms_event * 1e3,
+                        "gbs": byts / (ms * 1e-3) / 1e9, "bound": "hbm",
+                        "frac": byts / (ms * 1e-3) / 1e9 / hbm,
+                        "tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12})
+        del bs
+    return res
+
+
+def quantize_records(dev, gen, stream, r, cdim, steps, warmup, hbm, modes=(0, 1)):
+    """The 128x128 block quantizer on an FP32 [r, cdim] input rotated beyond L2:
+    read 4 B + write 1 B per element plus the scales."""
+    import torch
+    import block_quantize_gb300 as bq
+    copies = max(1, -(-3 * L2_BYTES // (r * cdim * 5)))
+    xs = [torch.randn((r, cdim), generator=gen, device=dev) for _ in range(copies)]
+    q = torch.empty((r, cdim), dtype=torch.uint8, device=dev)
+    s_ = torch.empty((-(-r // 128), -(-cdim // 128)), dtype=torch.float32, device=dev)
+    res = []
+    for mode in modes:
+        fns = [lambda x=x: bq.dg_quantize_fp8_block(x, mode, q, s_) for x in xs]
+        ms = statistics.median(_time_each(stream, fns, steps, warmup))
+        _check_status(bq, "quantizer")
+        byts = r * cdim * 5 + s_.numel() * 4
+        res.append({"rows": r, "cols": cdim, "scales": "ue8m0" if mode else "fp32", "us": ms * 1e3,
+                    "gbs": byts / (ms * 1e-3) / 1e9, "bound": "hbm",
+                    "frac": byts / (ms * 1e-3) / 1e9 / hbm})
+    del xs
+    return res
+
+
+def grouped_record(dev, gen, stream, steps, warmup, fp8_peak, mode=0):
+    """The M-grouped MoE GEMM: 8 experts, K = 4096, N = 11008, 4096 tokens
+    routed top-2 with seed-0 group sizes, each group padded to 128 rows."""
+    import torch
+    import block_quantize_gb300 as bq
+    mo = synthetic.MOE
+    sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
+    m_idx, _ = synthetic.moe_layout(sizes)
+    m_tot, k, n, g = m_idx.size, mo["hidden"], mo["intermediate"], mo["experts"]
+    qa, sa = _rand_fp8((m_tot, k), dev, gen, mode)
+    qb, sb = _rand_fp8((g * n, k), dev, gen, mode)
+    qb = qb.view(g, n, k)
+    sb = sb.view(g, -1, k // 128)
+    mi = torch.from_numpy(m_idx).to(dev)
+    c = torch.empty((m_tot, n), dtype=torch.bfloat16, device=dev)
+    ms = statistics.median(_time_each(
+        stream, [lambda: bq.dg_fp8_grouped_gemm_contiguous(c, qa, qb, sa, sb, mi, mode)], steps, warmup))
+    _check_status(bq, "grouped GEMM")
+    useful = 2.0 * int(sizes.sum()) * n * k
+    executed = 2.0 * m_tot * n * k
+    return {"M_tot": m_tot, "N": n, "K": k, "G": g, "scales": "ue8m0" if mode else "fp32", "us": ms * 1e3,
+            "tflops_useful": useful / (ms * 1e-3) / 1e12,
+            "tflops_executed": executed / (ms * 1e-3) / 1e12, "bound": "tensor",
+            "frac": executed / (ms * 1e-3) / 1e12 / fp8_peak}
+
+
+def _check_status(bq, what):
+    st = bq.dg_get_device_status()
+    if st != bq.DG_OK:
+        raise RuntimeError(f"{what}: device status {bq.dg_status_string(st)}")
+
+
+def config_records(dev, gen, stream, fp8_peak, hbm):
+    """Bounded timings of the metric's other workloads for the benchmark line."""
+    steps, warmup = 10, 3
+    q = quantize_records(dev, gen, stream, *synthetic.QUANT_SHAPE, steps, warmup, hbm)
+    small = small_records(dev, gen, stream, steps, warmup, hbm)
+    grouped = [grouped_record(dev, gen, stream, steps, warmup, fp8_peak, mode) for mode in (0, 1)]
+    squares = []
+    for mode in (0, 1):
+        squares += gemm_records(dev, gen, stream, [(s_, s_, s_) for s_ in synthetic.SQUARES[:2]], mode,
+                                steps, warmup, fp8_peak)
+    tiny = gemm_records(dev, gen, stream, [synthetic.TINY], 0, steps, warmup, fp8_peak)
+    tiny[0]["bound"] = "latency"
+    return {"quantize_16384x7168": q, "small_m_decode": small, "grouped_moe": grouped,
+            "square": squares, "tiny": tiny,
+            "timing": f"CUDA events, median of {steps} launches after {warmup} warm-up launches; "
+                      "decode shapes replayed from a CUDA graph; inputs rotated beyond L2"}
+
+
 def run_aux(args):
     import torch
     import block_quantize_gb300 as bq
@@ -481,54 +628,13 @@ def run_aux(args):
         else:
             mode = 1 if parts and parts[0] == "ue8m0" else 0
             shapes_ = [(s_, s_, s_) for s_ in synthetic.SQUARES]
-        res = []
-        for (m, n, k) in shapes_:
-            qa, sa = _rand_fp8((m, k), dev, gen, mode)
-            copies = max(1, min(8, -(-3 * L2_BYTES // (n * k))))
-            bs = [_rand_fp8((n, k), dev, gen, mode) for _ in range(copies)]
-            c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-            fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb, mode) for qb, sb in bs]
-            ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
-            tf = 2.0 * m * n * k / (ms * 1e-3) / 1e12
-            byts = m * k + n * k + 2 * m * n + 4 * (-(-m // 128) + -(-n // 128)) * (k // 128)
-            res.append({"M": m, "N": n, "K": k, "mode": mode, "us": ms * 1e3, "tflops": tf,
-                        "frac_fp8_burst": tf / fp8_peak, "gbs": byts / (ms * 1e-3) / 1e9})
-            del bs, qa, sa, c
-        out["results"] = res
+        out["results"] = gemm_records(dev, gen, stream, shapes_, mode, args.steps, args.warmup, fp8_peak)
     elif kind == "small":
-        res = []
-        for n, k in synthetic.SMALL_NK:
-            copies = max(1, -(-3 * L2_BYTES // (n * k)))
-            bs = [_rand_fp8((n, k), dev, gen, 0) for _ in range(copies)]
-            for m in synthetic.SMALL_M:
-                qa, sa = _rand_fp8((m, k), dev, gen, 0)
-                c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-                fns = [lambda qb=qb, sb=sb: bq.dg_fp8_gemm_nt(c, qa, qb, sa, sb) for qb, sb in bs]
-                ms_event = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
-                # Launches of a few microseconds: time them back to back from a
-                # CUDA graph (rotating B copies, so every launch reads HBM).
-                ms = _time_graph(stream, fns * max(1, 24 // len(fns)), max(args.steps, 10))
-                byts = m * k + n * k + 2 * m * n + 4 * (-(-m // 128) + -(-n // 128)) * (k // 128)
-                res.append({"M": m, "N": n, "K": k, "us": ms * 1e3, "us_single_launch": ms_event * 1e3,
-                            "gbs": byts / (ms * 1e-3) / 1e9,
-                            "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm,
-                            "tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12})
-            del bs
-        out["results"] = res
+        ms_ = [int(v) for v in spec.split(",")] if spec else None
+        out["results"] = small_records(dev, gen, stream, args.steps, args.warmup, hbm, ms_)
     elif kind == "quantize":
         r, cdim = (int(v) for v in (spec or "16384,7168").split(","))
-        copies = max(1, -(-3 * L2_BYTES // (r * cdim * 5)))
-        xs = [torch.randn((r, cdim), generator=gen, device=dev) for _ in range(copies)]
-        q = torch.empty((r, cdim), dtype=torch.uint8, device=dev)
-        s_ = torch.empty((-(-r // 128), -(-cdim // 128)), dtype=torch.float32, device=dev)
-        res = []
-        for mode in (0, 1):
-            fns = [lambda x=x: bq.dg_quantize_fp8_block(x, mode, q, s_) for x in xs]
-            ms = statistics.median(_time_each(stream, fns, args.steps, args.warmup))
-            byts = r * cdim * 5 + s_.numel() * 4
-            res.append({"rows": r, "cols": cdim, "mode": mode, "us": ms * 1e3,
-                        "gbs": byts / (ms * 1e-3) / 1e9, "frac_hbm": byts / (ms * 1e-3) / 1e9 / hbm})
-        out["results"] = res
+        out["results"] = quantize_records(dev, gen, stream, r, cdim, args.steps, args.warmup, hbm)
     elif kind == "quantize1x128":
         # Row-wise (1x128) activation quantizer, FP32 and bfloat16 inputs.
         r, cdim = (int(v) for v in (spec or "16384,7168").split(","))
@@ -629,24 +735,8 @@ def run_aux(args):
                            "tflops": fl / (ms * 1e-3) / 1e12,
                            "frac_fp8_burst": fl / (ms * 1e-3) / 1e12 / fp8_peak}]
     elif kind == "grouped":
-        mo = synthetic.MOE
-        sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
-        m_idx, _ = synthetic.moe_layout(sizes)
-        m_tot, k, n, g = m_idx.size, mo["hidden"], mo["intermediate"], mo["experts"]
-        qa, sa = _rand_fp8((m_tot, k), dev, gen, 0)
-        qb, sb = _rand_fp8((g * n, k), dev, gen, 0)
-        qb = qb.view(g, n, k)
-        sb = sb.view(g, -1, k // 128)
-        mi = torch.from_numpy(m_idx).to(dev)
-        c = torch.empty((m_tot, n), dtype=torch.bfloat16, device=dev)
-        ms = _time_each(stream, [lambda: bq.dg_fp8_grouped_gemm_contiguous(c, qa, qb, sa, sb, mi)],
-                        args.steps, args.warmup)[0]
-        useful = 2.0 * int(sizes.sum()) * n * k
-        executed = 2.0 * m_tot * n * k
-        out["results"] = [{"M_tot": m_tot, "N": n, "K": k, "G": g, "us": ms * 1e3,
-                           "tflops_useful": useful / (ms * 1e-3) / 1e12,
-                           "tflops_executed": executed / (ms * 1e-3) / 1e12,
-                           "frac_fp8_burst": executed / (ms * 1e-3) / 1e12 / fp8_peak}]
+        mode = 1 if spec == "ue8m0" else 0
+        out["results"] = [grouped_record(dev, gen, stream, args.steps, args.warmup, fp8_peak, mode)]
     else:
         raise SystemExit(f"unknown workload {args.workload}")
     if bq.dg_get_device_status() != bq.DG_OK:
@@ -662,6 +752,8 @@ def main():
                    help="timed steps (default 400 for this library's kernels, 20 for the CPU reference)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-configs", dest="configs", action="store_false",
+                   help="leave out the bounded per-config records of the line")
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
                         "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K] | "

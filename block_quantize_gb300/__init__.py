@@ -53,6 +53,7 @@ DG_ERR_MISALIGNED = 3
 DG_ERR_CUDA = 4
 DG_ERR_NO_DEVICE = 5
 DG_ERR_TIMEOUT = 6
+DG_ERR_BAD_GROUP = 7
 DG_SCALE_FP32 = 0
 DG_SCALE_UE8M0 = 1
 DG_INPUT_FP32 = 0

@@ -140,6 +140,7 @@ DG_API const char* dg_status_string(int status) {
     case DG_ERR_CUDA: return "CUDA runtime error or failed launch";
     case DG_ERR_NO_DEVICE: return "no usable CUDA device (sm_103 required)";
     case DG_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    case DG_ERR_BAD_GROUP: return "an M-grouped call met an expert id >= num_groups (those blocks were written as zeros)";
     default: return "unknown status";
   }
 }
@@ -404,11 +405,12 @@ DG_API int dg_get_device_status(void* stream) {
     return DG_ERR_CUDA;
   }
   unsigned int word = 0;
-  if (dg::read_and_clear_status(&word) != cudaSuccess) {
+  if (dg::read_and_clear_status(&word, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }
-  return (word & 1u) ? DG_ERR_TIMEOUT : DG_OK;
+  if (word & dg::kStatusTimeout) return DG_ERR_TIMEOUT;
+  return (word & dg::kStatusBadGroup) ? DG_ERR_BAD_GROUP : DG_OK;
 }
 
 DG_API int dg_selftest_wait_timeout(int64_t limit_ns, void* stream) {

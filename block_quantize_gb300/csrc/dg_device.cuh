@@ -6,10 +6,9 @@
 #include <cuda.h>
 #include <cstdint>
 
-namespace dg {
+#include "dg_internal.h"
 
-// Per-device status word; kernels OR a code into it when a bounded wait runs out.
-constexpr unsigned int kStatusTimeout = 1u;
+namespace dg {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -9,6 +9,11 @@
 
 namespace dg {
 
+// Bits of the per-device status word: kernels OR one in when a bounded wait
+// runs out, or when an M-grouped call meets an expert id outside [0, num_groups).
+constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusBadGroup = 2u;
+
 // Launch a kernel with programmatic dependent launch allowed (and a cluster
 // of cluster_x CTAs when cluster_x > 0). The kernel may then begin while the
 // previous work on the stream finishes, so it must execute griddepcontrol.wait
@@ -102,9 +107,10 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream);
 bool gemv_supported(const GemmProblem& p);
 int launch_gemv(const GemmProblem& p, cudaStream_t stream);
 
-// Reads and clears the current device's status word (a bitmask of kernel
-// timeouts). Returns the CUDA error of the copy.
-cudaError_t read_and_clear_status(unsigned int* out);
+// Takes and clears the current device's status word (kStatusTimeout,
+// kStatusBadGroup bits) in one atomic step on `stream`, then waits for the
+// stream. Returns the CUDA error of the launch or the copy.
+cudaError_t read_and_clear_status(unsigned int* out, cudaStream_t stream);
 
 // Launches one block that waits on a barrier nothing arrives at, so that its
 // bounded wait runs out after limit_ns.

@@ -49,6 +49,7 @@
 namespace dg {
 
 __device__ unsigned int g_status_word;
+__device__ unsigned int g_status_taken;  // the word's value at the last read-and-clear
 
 namespace {
 
@@ -76,6 +77,7 @@ struct GemmArgs {
   int num_mb;      // ceil(M / 128)
   int num_nb;      // ceil(N / BN)
   int nbs;         // ceil(N / 128): rows of one expert's sb
+  int num_groups;  // experts of an M-grouped call (ids outside [0, num_groups) are skipped)
   int num_stages;
   uint32_t a_stage_bytes;  // smem bytes of one A stage (>= the A box, 1024-aligned)
   uint32_t a_box_bytes;    // bytes one A TMA box delivers
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       int g = 0;
       if constexpr (kGrouped) {
         g = block_group(args.m_indices, mb, lane);
-        if (g < 0) continue;
+        if (g < 0 || g >= args.num_groups) continue;
       }
       for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
         const uint32_t stage = it % S;
@@ -280,7 +282,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       if constexpr (kGrouped) {
-        if (block_group(args.m_indices, mb, lane) < 0) continue;
+        const int g = block_group(args.m_indices, mb, lane);
+        if (g < 0 || g >= args.num_groups) continue;
       }
       for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
         if (it % C::kIssuers != me) continue;
@@ -340,8 +343,13 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       int g = 0;
-      if constexpr (kGrouped) g = block_group(args.m_indices, mb, lane);
-      const bool skip = kGrouped && g < 0;
+      if constexpr (kGrouped) {
+        g = block_group(args.m_indices, mb, lane);
+        // An id past the last expert: the block is written as zeros, no B or sb
+        // of that id is read, and the status word records it.
+        if (g >= args.num_groups && ew == 0 && lane == 0) atomicOr(status, kStatusBadGroup);
+      }
+      const bool skip = kGrouped && (g < 0 || g >= args.num_groups);
       const int col0 = nb * BN + part * kCols;
       const bool part_valid = col0 < args.N;
       const int sb_block = min(col0 / kBK, args.nbs - 1);
@@ -544,6 +552,10 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
   }
 }
 
+// Takes the status word and clears it in one atomic step, so that a bit another
+// stream's kernel sets at the same time lands either in this read or the next.
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status_word, 0u); }
+
 // dst[i] = v for i < n (grid-stride).
 __global__ void fill_f32_kernel(float* dst, int64_t n, float v) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -670,6 +682,7 @@ int run_gemm(const GemmProblem& p, cudaStream_t stream, int dev, int sms) {
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
   args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
+  args.num_groups = p.num_groups;
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
   // A box: all 128 rows, or the valid rows (multiple of 8) when M is small.
@@ -844,11 +857,15 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   }
 }
 
-cudaError_t read_and_clear_status(unsigned int* out) {
-  unsigned int zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_status_word, sizeof(unsigned int));
+cudaError_t read_and_clear_status(unsigned int* out, cudaStream_t stream) {
+  static std::mutex mu;  // one snapshot slot per device: one reader at a time
+  std::lock_guard<std::mutex> lock(mu);
+  status_take_kernel<<<1, 1, 0, stream>>>();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_status_word, &zero, sizeof(unsigned int));
+  e = cudaMemcpyFromSymbolAsync(out, g_status_taken, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
 }
 
 cudaError_t launch_fill_f32(float* dst, int64_t n, float v, cudaStream_t stream) {

@@ -36,7 +36,11 @@
  *   - Return value: a dg_status. No C++ exception crosses this boundary.
  *   - Timeouts: every wait inside a kernel is bounded; a wait that runs out sets
  *     a per-device status word and makes the kernel return early (its output is
- *     then undefined). dg_get_device_status() reads and clears that word.
+ *     then undefined). dg_get_device_status() reads and clears that word. The
+ *     compute calls return before their kernels run, so they cannot report
+ *     this: a caller that must know whether a result is valid calls
+ *     dg_get_device_status() after it (the tests and the benchmark do so after
+ *     each check and each timed region).
  */
 #ifndef DGFP8_H_
 #define DGFP8_H_
@@ -53,7 +57,7 @@ extern "C" {
 #define DG_API __attribute__((visibility("default")))
 #endif
 
-#define DG_ABI_VERSION 5u
+#define DG_ABI_VERSION 6u
 
 typedef enum {
     DG_OK = 0,
@@ -62,7 +66,8 @@ typedef enum {
     DG_ERR_MISALIGNED = 3,         /* pointer or stride breaks a 16-byte (TMA) rule */
     DG_ERR_CUDA = 4,               /* a CUDA runtime call or a launch failed */
     DG_ERR_NO_DEVICE = 5,          /* no CUDA device, or the device is not sm_103 */
-    DG_ERR_TIMEOUT = 6             /* a bounded in-kernel wait ran out (see above) */
+    DG_ERR_TIMEOUT = 6,            /* a bounded in-kernel wait ran out (see above) */
+    DG_ERR_BAD_GROUP = 7           /* an M-grouped call met an expert id >= num_groups */
 } dg_status;
 
 typedef enum {
@@ -180,7 +185,9 @@ DG_API int dg_fp8_gemm_nt_1x128(void *c, int64_t ld_c,
  *              padding row. Rows of one 128-row block carry one expert id or -1
  *              (each expert's rows start on a multiple of 128). Output rows with
  *              -1 are written as zeros; a block made only of -1 rows is zero.
- *              Ids >= num_groups make that block's result undefined.
+ *              A block whose id is >= num_groups reads no B or sb, is written
+ *              as zeros, and sets the status that dg_get_device_status()
+ *              then reports as DG_ERR_BAD_GROUP.
  * Needs M_tot % 128 == 0 and the alignment rules of dg_fp8_gemm_nt (with
  * ld_b = K). */
 DG_API int dg_fp8_grouped_gemm_contiguous(void *c, int64_t ld_c,
@@ -283,9 +290,13 @@ DG_API int dg_fp8_k_grouped_gemm_tn(void *c, int64_t ld_c,
                                     int num_groups, const int64_t *k_sizes,
                                     int64_t M, int64_t N, int scale_mode, void *stream);
 
-/* Synchronize `stream`, then read and clear the current device's status word.
- * Returns DG_ERR_TIMEOUT if a kernel's bounded wait ran out since the last
- * call, DG_ERR_CUDA if the stream reports an error, else DG_OK. */
+/* Synchronize `stream`, then take and clear the current device's status word
+ * in one atomic step (a kernel on another stream that sets it meanwhile is
+ * reported by this call or the next, never lost). Returns DG_ERR_TIMEOUT if a
+ * kernel's bounded wait ran out since the last call, else DG_ERR_BAD_GROUP if
+ * an M-grouped call met an expert id >= num_groups, DG_ERR_CUDA if the stream
+ * reports an error, else DG_OK. The word is one per device, shared by all
+ * streams: it does not say which call set it. */
 DG_API int dg_get_device_status(void *stream);
 
 /* Self-test of the timeout path: launches one block whose wait on a barrier

@@ -48,6 +48,23 @@ def sample_rows(m, count, seed=0):
     return np.unique(np.concatenate([fixed, rest])).astype(np.int64)
 
 
+def rows_per_block(m, block=128, seed=0, valid=None):
+    """One random row in every `block`-row block of [0, m) (the tiles of every
+    CTA of a launch), plus the first and last rows of the first and the final
+    block. With `valid` (a boolean mask) the random row is drawn from the valid
+    rows of its block, and blocks without one are skipped."""
+    rng = np.random.default_rng(seed)
+    rows = [0, min(block - 1, m - 1), (m - 1) // block * block, m - 1]
+    for b0 in range(0, m, block):
+        cand = np.arange(b0, min(b0 + block, m))
+        if valid is not None:
+            cand = cand[valid[cand]]
+        if cand.size:
+            rows.append(int(rng.choice(cand)))
+    rows = np.unique(np.asarray(rows, np.int64))
+    return rows if valid is None else rows[valid[rows]]
+
+
 def _expand_scales(s, m, n, block_rows):
     s = np.asarray(s, np.float64)
     if block_rows == 1:

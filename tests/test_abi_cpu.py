@@ -25,11 +25,12 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_strings_alignment(L):
-    assert bq.dg_get_abi_version() == 5
+    assert bq.dg_get_abi_version() == 6
     assert bq.dg_get_mk_alignment_for_contiguous_layout() == 128
-    for s in range(7):
+    for s in range(8):
         assert bq.dg_status_string(s)
     assert bq.dg_status_string(99) == "unknown status"
+    assert "expert id" in bq.dg_status_string(bq.DG_ERR_BAD_GROUP)
 
 
 def test_num_sms_knob(L):

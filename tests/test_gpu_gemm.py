@@ -10,7 +10,7 @@ import torch
 
 import block_quantize_gb300 as bq
 import synthetic
-from parity import assert_within_bound, device, host, sample_rows, to_dev
+from parity import assert_within_bound, device, host, rows_per_block, sample_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -105,7 +105,7 @@ def test_llm_projection_shapes(oracle_mod, nk):
     m = synthetic.LLM_M
     qa, sa, qb, sb = _operands(oracle_mod, m, n, k, synthetic.seed_for(2, synthetic.LLM_NK.index(nk)),
                                dist="lognormal")
-    _check(oracle_mod, qa, sa, qb, sb, rows=sample_rows(m, 40, seed=n), what=f"{m}x{n}x{k}")
+    _check(oracle_mod, qa, sa, qb, sb, rows=rows_per_block(m, 128, seed=n), what=f"{m}x{n}x{k}")
 
 
 @pytest.mark.parametrize("m", synthetic.SMALL_M)
@@ -123,8 +123,9 @@ def test_square_shapes(oracle_mod, size, mode):
     qa, sa, qb, sb = _operands(oracle_mod, size, size, size, synthetic.seed_for(5, size), mode)
     if mode == 1:
         assert np.all(np.frexp(sa)[0] == 0.5) and np.all(np.frexp(sb)[0] == 0.5)
-    count = {4096: 24, 8192: 12, 16384: 6}[size]
-    _check(oracle_mod, qa, sa, qb, sb, rows=sample_rows(size, count, seed=size), mode=mode,
+    # One row in every 128-row block: every CTA of every 256-row pair tile, and
+    # the first and last rows of the final tile.
+    _check(oracle_mod, qa, sa, qb, sb, rows=rows_per_block(size, 128, seed=size + mode), mode=mode,
            what=f"{size}^3 mode {mode}")
 
 

@@ -3,13 +3,15 @@ oracle, through the C ABI (pzsr.cn "DeepGEMM: GPU上的高效BLAS内核库解析
 §3.2, §3.3: grouped GEMM along M, rows aligned to
 get_mk_alignment_for_contiguous_layout()). Operands come from the oracle's
 quantizer; padding rows (index -1) must come out as zeros."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import block_quantize_gb300 as bq
 import synthetic
-from parity import assert_within_bound, device, to_dev
+from parity import assert_within_bound, device, rows_per_block, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -61,19 +63,24 @@ def test_small_groups_with_empty_expert_and_padding(oracle_mod, mode):
     assert torch.count_nonzero(c[torch.as_tensor(m_idx < 0, device=c.device)]) == 0
 
 
-def test_moe_8_experts_11008x4096(oracle_mod):
-    """8 experts, K = 4096 hidden, N = 11008 intermediate, 4096 tokens top-2."""
+@pytest.mark.parametrize("mode", [0, 1])
+def test_moe_8_experts_11008x4096(oracle_mod, mode):
+    """8 experts, K = 4096 hidden, N = 11008 intermediate, 4096 tokens top-2,
+    with FP32 and with power-of-two block scales."""
     mo = synthetic.MOE
     a, b, m_idx, sizes = synthetic.moe_inputs(seed=0, experts=mo["experts"], tokens=mo["tokens"],
                                                topk=mo["topk"], hidden=mo["hidden"],
                                                intermediate=mo["intermediate"])
     assert m_idx.size == 8960 and list(sizes) == [1033, 1551, 36, 6, 873, 2462, 1027, 1204]
-    qa, sa = oracle_mod.quantize(a)
-    qb, sb = _quantize_experts(oracle_mod, b)
-    c = _run(qa, sa, qb, sb, m_idx)
-    rows = _rows_per_group(m_idx, 6, seed=1)
+    qa, sa = oracle_mod.quantize(a, mode)
+    qb, sb = _quantize_experts(oracle_mod, b, mode)
+    c = _run(qa, sa, qb, sb, m_idx, mode)
+    # Every 128-row block (each expert's blocks, its partial last block) plus
+    # each expert's first and last rows.
+    rows = np.union1d(_rows_per_group(m_idx, 6, seed=1), rows_per_block(m_idx.size, 128, seed=2, valid=m_idx >= 0))
     ref, mag = oracle_mod.grouped_gemm_contiguous(qa, sa, qb, sb, m_idx, rows=rows)
     assert_within_bound(c[torch.as_tensor(rows, device=c.device)], ref, mag, "MoE 8x11008x4096")
+    assert torch.count_nonzero(c[torch.as_tensor(m_idx < 0, device=c.device)]) == 0
 
 
 def test_grouped_few_sms(oracle_mod):
@@ -112,3 +119,33 @@ def test_grouped_matches_dense_bitwise(oracle_mod):
         bq.dg_fp8_gemm_nt(cd, to_dev(qa[lo:hi], dev), to_dev(qb[g], dev),
                           to_dev(sa[lo // 128:hi // 128], dev), to_dev(sb[g], dev))
         assert torch.equal(cd.view(torch.int16), c[lo:hi].view(torch.int16))
+
+
+def test_expert_id_past_the_last_group_is_zeroed_and_reported(oracle_mod):
+    """A 128-row block whose expert id equals num_groups reads no B or sb of
+    that id, comes out as zeros, and sets DG_ERR_BAD_GROUP. B and sb are
+    allocated for one expert more than num_groups, so that even a read of the
+    bad id would stay inside the allocations."""
+    dev = device()
+    k, n, g = 256, 256, 2
+    m_idx = np.concatenate([np.full(128, 0, np.int32), np.full(128, g, np.int32),
+                            np.full(100, 1, np.int32), np.full(28, -1, np.int32)])
+    a = synthetic.lognormal_rows((m_idx.size, k), seed=211)
+    b = synthetic.lognormal_rows(((g + 1) * n, k), seed=212).reshape(g + 1, n, k)
+    qa, sa = oracle_mod.quantize(a)
+    qb, sb = _quantize_experts(oracle_mod, b)
+    c = torch.full((m_idx.size, n), float("nan"), dtype=torch.bfloat16, device=dev)
+    qb_d, sb_d = to_dev(qb, dev), to_dev(sb, dev)
+    rc = bq.lib().dg_fp8_grouped_gemm_contiguous(
+        ctypes.c_void_p(c.data_ptr()), n, ctypes.c_void_p(to_dev(qa, dev).data_ptr()), k,
+        ctypes.c_void_p(to_dev(sa, dev).data_ptr()), ctypes.c_void_p(qb_d.data_ptr()),
+        ctypes.c_void_p(sb_d.data_ptr()), g, ctypes.c_void_p(to_dev(m_idx, dev).data_ptr()),
+        m_idx.size, n, k, 0, ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    assert rc == bq.DG_OK
+    assert bq.dg_get_device_status() == bq.DG_ERR_BAD_GROUP
+    assert bq.dg_get_device_status() == bq.DG_OK          # taken and cleared
+    got = c.float().cpu().numpy()
+    assert np.all(got[128:256] == 0.0)
+    good = np.where(m_idx == g, -1, m_idx).astype(np.int32)
+    ref, mag = oracle_mod.grouped_gemm_contiguous(qa, sa, qb[:g], sb[:g], good)
+    assert_within_bound(c, ref, mag, "grouped with a bad expert id")
