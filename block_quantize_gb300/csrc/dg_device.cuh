@@ -105,6 +105,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Expert of 128-row block mb of an M-grouped call: the largest id among its
+// rows (rows carry one id or -1 for padding). Warp-collective: the 32 lanes
+// read 4 ids each (m_indices 16-byte aligned, the block inside the array).
+__device__ __forceinline__ int m_block_group(const int32_t* m_indices, int mb, int lane) {
+  const int4 v = __ldg(reinterpret_cast<const int4*>(m_indices + static_cast<int64_t>(mb) * 128) + lane);
+  const int m = max(max(v.x, v.y), max(v.z, v.w));
+  return __reduce_max_sync(0xFFFFFFFFu, m);
+}
+
 // Two FP32 fused multiply-adds in one instruction (sm_100+ f32x2): each lane
 // of the pair is fmaf(s, p, acc) rounded to nearest, as two scalar FFMAs are.
 __device__ __forceinline__ uint64_t f32x2(uint32_t lo, uint32_t hi) {
@@ -245,6 +254,16 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// 4-D form of the same (M-grouped operands: the last coordinate is the expert).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
 // 2-D form of the same.

@@ -146,13 +146,6 @@ __device__ __forceinline__ void tile_coords(int t, int num_mb, int num_nb, int& 
   nb = r / gm;
 }
 
-// Expert of 128-row block mb: the largest id among its rows (rows carry one id
-// or -1). Warp-collective: 32 lanes read 4 ids each.
-__device__ __forceinline__ int block_group(const int32_t* m_indices, int mb, int lane) {
-  const int4 v = __ldg(reinterpret_cast<const int4*>(m_indices + static_cast<int64_t>(mb) * kBM) + lane);
-  const int m = max(max(v.x, v.y), max(v.z, v.w));
-  return __reduce_max_sync(0xFFFFFFFFu, m);
-}
 
 // Bounded wait that ignores the abort flag (used while draining).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -238,7 +231,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       int g = 0;
       if constexpr (kGrouped) {
-        g = block_group(args.m_indices, mb, lane);
+        g = m_block_group(args.m_indices, mb, lane);
         if (g < 0 || g >= args.num_groups) continue;
       }
       for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
@@ -282,7 +275,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       int mb, nb;
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       if constexpr (kGrouped) {
-        const int g = block_group(args.m_indices, mb, lane);
+        const int g = m_block_group(args.m_indices, mb, lane);
         if (g < 0 || g >= args.num_groups) continue;
       }
       for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
@@ -344,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
       tile_coords(t, args.num_mb, args.num_nb, mb, nb);
       int g = 0;
       if constexpr (kGrouped) {
-        g = block_group(args.m_indices, mb, lane);
+        g = m_block_group(args.m_indices, mb, lane);
         // An id past the last expert: the block is written as zeros, no B or sb
         // of that id is read, and the status word records it.
         if (g >= args.num_groups && ew == 0 && lane == 0) atomicOr(status, kStatusBadGroup);
@@ -832,7 +825,9 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   // Decode shapes: one row streams B (gemv.cu); M <= 128, cluster split-K.
   if (!block_n_override() && gemv_supported(p)) return launch_gemv(p, stream);
   if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
-  if (!block_n_override() && p.m_indices == nullptr && p.M > kBM) {
+  // Dense M > 128 and every M-grouped call: CTA pairs (the grouped calls fall
+  // back to the 1-SM kernel below when fewer than two SMs are allowed).
+  if (!block_n_override() && (p.m_indices != nullptr || p.M > kBM)) {
     const int r = launch_gemm_pair(p, stream);
     if (r != DG_ERR_UNSUPPORTED_SHAPE) return r;
   }

@@ -29,6 +29,13 @@
 //     rounded like fmaf). After the last K block each warp rounds its 32 x 32
 //     boxes to bf16 and writes them with TMA stores clipped at the M and N edges;
 //   * pairs are persistent over the 256x128 tiles in a grouped raster.
+// M-grouped calls (MoE experts, pzsr.cn page §2.3, §3.2) run on the same
+// kernels: both 128-row halves of a pair tile multiply one B, so a pair row
+// whose two blocks belong to one expert is one unit, and a pair row whose
+// blocks belong to different experts (or to an expert and padding) becomes
+// two units, each with one CTA keeping its rows and the other discarding its
+// (see pair_unit). Blocks of padding rows only, or of an id past the last
+// expert, run no MMAs and are written as zeros.
 // Every mbarrier wait is bounded; on a timeout the CTA raises its abort flag,
 // records it in the device status word, drains what it has in flight, frees
 // TMEM and leaves through the final cluster barrier.
@@ -104,8 +111,18 @@ struct PairArgs {
 struct PairArgsQ : PairArgs {
   RequantOut rq;     // E4M3 output and scales
 };
-template <bool kQ>
-using PairArgsT = std::conditional_t<kQ, PairArgsQ, PairArgs>;
+// M-grouped calls add the expert of each row (-1: padding) and the number of
+// experts (ids outside [0, num_groups) run no MMAs). Separate types again, so
+// that the dense kernels keep their argument layout.
+struct PairGroups {
+  const int32_t* m_indices;
+  int num_groups;
+};
+struct PairArgsG : PairArgs, PairGroups {};
+struct PairArgsQG : PairArgsQ, PairGroups {};
+template <bool kQ, bool kG = false>
+using PairArgsT = std::conditional_t<kG, std::conditional_t<kQ, PairArgsQG, PairArgsG>,
+                                     std::conditional_t<kQ, PairArgsQ, PairArgs>>;
 
 __device__ __forceinline__ void pair_tile_coords(int t, int num_pm, int num_nb, int& pm, int& nb) {
   const int per_group = kGroupPM * num_nb;
@@ -115,6 +132,81 @@ __device__ __forceinline__ void pair_tile_coords(int t, int num_pm, int num_nb, 
   const int r = t - grp * per_group;
   pm = first + r % gm;
   nb = r / gm;
+}
+
+// One unit of a pair's persistent work: pair row pm (A rows [256 pm, +256)),
+// N tile nb, the expert whose B the MMAs read, which CTAs keep their 128 rows
+// (bit r: CTA r writes its rows; the other CTA's rows are discarded), and
+// whether the unit runs MMAs at all (a block of padding rows only, or of an
+// id past the last expert, is written as zeros without them).
+// A unit of a pair's persistent work: pair row pm (A rows [256 pm, +256)) and
+// N tile nb. Dense calls run one slot per unit. M-grouped calls (both 128-row
+// halves of a pair MMA multiply one B, so one expert) look up the experts g0,
+// g1 of the row's blocks b0 = 2 pm and b1 = b0 + 1:
+//   * g0 == g1 (one expert, or both padding), or no block b1: one slot, the
+//     whole pair row with expert g0 (a missing b1 is discarded);
+//   * otherwise two slots, slot s covering block b_s with expert g_s: CTA s
+//     keeps its rows, the other CTA's half of the MMA result is discarded.
+// A slot whose expert is -1 (padding) or past the last expert runs no MMAs;
+// its kept rows are written as zeros.
+struct PairUnit {
+  int pm, nb;
+  int g0, g1;
+  int nslots;
+};
+struct PairSlot {
+  int g, keep;     // expert of the MMAs; bit r set: CTA r writes its 128 rows
+  bool mma, bad;   // the MMAs run; the expert id is past the last expert
+};
+
+__device__ __forceinline__ int pair_num_units(const PairArgs& a) { return a.num_pm * a.num_nb; }
+
+// The raw ids a unit's lookup reduces (4 per lane for each of b0, b1), loaded
+// one unit ahead so that their latency hides behind the current unit.
+struct UnitIds {
+  int4 v0, v1;
+};
+template <bool kGrouped, class Args>
+__device__ __forceinline__ UnitIds pair_unit_ids(int t, const Args& a, int lane) {
+  UnitIds r{make_int4(-1, -1, -1, -1), make_int4(-1, -1, -1, -1)};
+  if constexpr (kGrouped) {
+    if (t < pair_num_units(a)) {
+      int pm, nb;
+      pair_tile_coords(t, a.num_pm, a.num_nb, pm, nb);
+      const int4* ids = reinterpret_cast<const int4*>(a.m_indices);
+      r.v0 = __ldg(ids + static_cast<int64_t>(2 * pm) * 32 + lane);
+      if (2 * pm + 1 < a.num_mb) r.v1 = __ldg(ids + static_cast<int64_t>(2 * pm + 1) * 32 + lane);
+    }
+  }
+  return r;
+}
+// Unit t from its ids (warp-collective for M-grouped calls).
+template <bool kGrouped, class Args>
+__device__ __forceinline__ PairUnit pair_unit(int t, const Args& a, const UnitIds& ids) {
+  PairUnit u;
+  pair_tile_coords(t, a.num_pm, a.num_nb, u.pm, u.nb);
+  u.g0 = u.g1 = 0;
+  u.nslots = 1;
+  if constexpr (kGrouped) {
+    const int m0 = max(max(ids.v0.x, ids.v0.y), max(ids.v0.z, ids.v0.w));
+    const int m1 = max(max(ids.v1.x, ids.v1.y), max(ids.v1.z, ids.v1.w));
+    u.g0 = __reduce_max_sync(0xFFFFFFFFu, m0);
+    const bool has1 = 2 * u.pm + 1 < a.num_mb;
+    u.g1 = has1 ? __reduce_max_sync(0xFFFFFFFFu, m1) : u.g0;
+    u.nslots = (has1 && u.g1 != u.g0) ? 2 : 1;
+  }
+  return u;
+}
+template <bool kGrouped, class Args>
+__device__ __forceinline__ PairSlot pair_slot(const PairUnit& u, int slot, const Args& a) {
+  PairSlot s{0, 3, true, false};
+  if constexpr (kGrouped) {
+    s.g = slot == 0 ? u.g0 : u.g1;
+    s.keep = u.nslots == 1 ? 3 : (1 << slot);
+    s.bad = s.g >= a.num_groups;
+    s.mma = s.g >= 0 && !s.bad;
+  }
+  return s;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -181,7 +273,7 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
 // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA stores, clipped at M.
 // A box that crosses column N is written element by element instead: the
 // swizzled store clips N only to whole 16-byte chunks.
-template <int EC>
+template <int EC, int kBoxes = EC / 32>
 __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], const CUtensorMap& tmap_c,
                                                 const PairArgs& args, uint8_t* out_box, int row0, int col0,
                                                 int lane, bool& stores_issued) {
@@ -189,6 +281,10 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < EC / 32; ++h) {
+    if (kBoxes == 1 && h > 0) {  // one box, reused: its previous store must have read it
+      if (lane == 0 && stores_issued) bulk_wait_read_all();
+      __syncwarp();
+    }
     const int bcol = col0 + 32 * h;
     if (bcol + 32 > args.N) {
       const int row = row0 + lane;
@@ -203,7 +299,7 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
       }
       continue;
     }
-    uint8_t* box = out_box + h * kBoxBytes;
+    uint8_t* box = out_box + (kBoxes == 1 ? 0 : h) * kBoxBytes;
     uint8_t* my_row = box + lane * 64;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -216,6 +312,44 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
       pk.w = pack_bf16(v3.x, v3.y);
       *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) = pk;
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < args.M) {
+      tma_store_2d(&tmap_c, smem_u32(box), bcol, row0);
+      bulk_commit();
+      stores_issued = true;
+    }
+  }
+}
+
+// The same store for a row slice already rounded to bf16: pk[j] holds columns
+// col0 + 2 j and col0 + 2 j + 1; one staging box per warp, reused for the
+// second 32-column half once its first store has read it.
+__device__ __forceinline__ void store_packed_rows(const uint32_t (&pk)[32], const CUtensorMap& tmap_c,
+                                                  const PairArgs& args, uint8_t* box, int row0, int col0,
+                                                  int lane, bool& stores_issued) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int bcol = col0 + 32 * h;
+    if (bcol + 32 > args.N) {
+      const int row = row0 + lane;
+      if (row < args.M && bcol < args.N) {
+        uint16_t* crow = reinterpret_cast<uint16_t*>(args.c + static_cast<int64_t>(row) * args.ld_c);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (bcol + 2 * j < args.N) crow[bcol + 2 * j] = static_cast<uint16_t>(pk[h * 16 + j] & 0xFFFFu);
+          if (bcol + 2 * j + 1 < args.N) crow[bcol + 2 * j + 1] = static_cast<uint16_t>(pk[h * 16 + j] >> 16);
+        }
+      }
+      continue;
+    }
+    if (lane == 0 && stores_issued) bulk_wait_read_all();  // the box's previous store has read it
+    __syncwarp();
+    uint8_t* my_row = box + lane * 64;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(my_row + ((c ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(pk[h * 16 + 4 * c], pk[h * 16 + 4 * c + 1], pk[h * 16 + 4 * c + 2], pk[h * 16 + 4 * c + 3]);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && row0 < args.M) {
@@ -497,25 +631,55 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
 //     columns; they wait on the stage's `empty` barrier like the producers and
 //     arrive on its `full` barrier, which thus completes when both CTAs'
 //     operands and scales are in place;
-//   * warps 8-15: per tile, read the accumulator, release it, round to bf16
+//   * warps 8 on: per tile, read the accumulator, release it, round to bf16
 //     and store.
 // A stage past an odd number of K blocks holds a zero-filled K block that gets
 // no MMA and no scale.
+//
+// Two tile widths. 256x128 pair tiles (N = 128 MMAs, two accumulators of 128
+// columns alternating between tiles) serve every layout and the requantizing
+// epilogue. 256x256 pair tiles (N = 256 MMAs) serve bf16 output in the NT
+// layout: each MMA does twice the work per instruction and per byte of A read
+// from shared memory (per SM and K block 48 KB of operand reads and 32 KB of
+// TMA writes for 512 tensor cycles, against 32 + 24 KB for 256 cycles), at
+// the price of one 256-column accumulator, which the epilogue must read before
+// the next tile's first MMA.
+// Where the MMA reads the scale factors (probed on the GPU with exponents that
+// encode their TMEM position): every TMEM lane quadrant holds its own copy;
+// the factor of B column n (of A row m) sits in lane 32 q + n % 32 of column
+// n / 32 of the B (A) scale area. A 128-row scale block therefore fills four
+// columns uniformly: four B columns for 128-column tiles, eight (the tile's two
+// B blocks, both CTAs writing both) for 256-column tiles.
 // ---------------------------------------------------------------------------
-constexpr int kNatKbPerStage = 2;
-constexpr uint32_t kNatStageBytes = kNatKbPerStage * kStageBytes;  // A [2][128][128 B], B [2][64][128 B]
-constexpr uint32_t kNatAStageBytes = kNatKbPerStage * kABytes;
 constexpr int kNatMaxStages = 8;
-constexpr uint32_t kSfCols = 8;                        // 4 columns for A, 4 for B, per K block
-constexpr uint32_t kAccCols = 2 * kBN;                 // two tile accumulators
-constexpr uint32_t kIdescScaled = idesc_e4m3_block_scaled(2 * kBM, kBN);
-constexpr int kNatEpiWarps = 8;                        // 4 quadrants x 2 slices of 64 columns
 constexpr int kNatFirstEpiWarp = 8;
-constexpr int kNatThreads = 32 * (kNatFirstEpiWarp + kNatEpiWarps);
+
+template <int kBNs>
+struct NatCfg {
+  static_assert(kBNs == 128 || kBNs == 256, "pair tile width");
+  static constexpr int kNumAcc = kBNs == 256 ? 1 : 2;                   // tile accumulators in TMEM
+  static constexpr uint32_t kAccCols = kNumAcc * kBNs;
+  static constexpr uint32_t kBHalf = (kBNs / 2) * kBK;                   // this CTA's B rows per K block
+  // K blocks per stage: two (one 3-D box of each operand carries both), or one
+  // for the 256-column tiles, whose 64 KB double stages would leave room for
+  // only two of them next to the output staging (the count must be even).
+  static constexpr int kKbPerStage = kBNs == 256 ? 1 : 2;
+  static constexpr uint32_t kAStage = kKbPerStage * kABytes;
+  static constexpr uint32_t kStageBytes = kAStage + kKbPerStage * kBHalf;
+  static constexpr int kEpiWarps = kBNs / 16;                            // 4 quadrants x BN/64 slices of 64
+  static constexpr int kThreads = 32 * (kNatFirstEpiWarp + kEpiWarps);
+  static constexpr int kBoxes = kBNs == 256 ? 1 : 2;                     // bf16 staging boxes per warp
+  static constexpr uint32_t kIdesc = idesc_e4m3_block_scaled(2 * kBM, kBNs);
+  // Scale columns per K block: 4 for A, then 4 (or 8) for B; rounded to whole
+  // 8-column stores.
+  static constexpr uint32_t kSfCols = kBNs == 256 ? 16 : 8;
+  static_assert(kAccCols + kNatMaxStages * kKbPerStage * kSfCols <= 512, "TMEM");
+};
+template <int kBNs>
 __host__ __device__ constexpr uint32_t nat_out_bytes(bool requant) {
-  return requant ? requant_smem_bytes(kNatEpiWarps) : kNatEpiWarps * kBoxBytes * 2;
+  return requant ? requant_smem_bytes(NatCfg<kBNs>::kEpiWarps)
+                 : NatCfg<kBNs>::kEpiWarps * kBoxBytes * NatCfg<kBNs>::kBoxes;
 }
-static_assert(kAccCols + kNatMaxStages * kNatKbPerStage * kSfCols <= 512, "TMEM");
 
 // Biased exponent of a power-of-two FP32 scale = its UE8M0 code (2^-127,
 // stored as an FP32 subnormal, has code 0), replicated into four bytes.
@@ -523,22 +687,24 @@ __device__ __forceinline__ uint32_t ue8m0_word(float s) {
   return 0x01010101u * ((__float_as_uint(s) >> 23) & 0xFFu);
 }
 
-template <bool kQ, bool kNT>
-__global__ void __launch_bounds__(kNatThreads, 1)
+template <bool kQ, bool kNT, bool kGrouped, int kBNs>
+__global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
     fp8_gemm_pair_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
-                                const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ> args) {
+                                const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ, kGrouped> args) {
+  using NC = NatCfg<kBNs>;
+  static_assert(kBNs == 128 || (!kQ && kNT), "256-column pair tiles: bf16 output, NT layout");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = args.num_stages;
   uint8_t* ring = smem;
-  uint8_t* smem_out = smem + static_cast<size_t>(S) * kNatStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + nat_out_bytes(kQ));
+  uint8_t* smem_out = smem + static_cast<size_t>(S) * NC::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_out + nat_out_bytes<kBNs>(kQ));
   uint64_t* full_bar = bars;                       // even CTA: operands and scales of both CTAs
   uint64_t* empty_bar = bars + kNatMaxStages;      // the stage's MMAs are done
-  uint64_t* tfull_bar = bars + 2 * kNatMaxStages;  // [2] the tile's accumulator is final
-  uint64_t* tempty_bar = tfull_bar + 2;            // [2] even CTA: both epilogues read it
+  uint64_t* tfull_bar = bars + 2 * kNatMaxStages;  // [kNumAcc] the tile's accumulator is final
+  uint64_t* tempty_bar = tfull_bar + 2;            // [kNumAcc] even CTA: both epilogues read it
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -552,19 +718,19 @@ __global__ void __launch_bounds__(kNatThreads, 1)
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
   const uint64_t limit = args.wait_limit_ns;
   unsigned int* status = args.status;
-  const int nst = (args.num_kb + kNatKbPerStage - 1) / kNatKbPerStage;  // stages per tile
+  const int nst = (args.num_kb + NC::kKbPerStage - 1) / NC::kKbPerStage;  // stages per tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1 + 2 * 4);  // producer (with bytes) + 4 scale writers per CTA
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NC::kNumAcc; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), nst >= 2 ? 2 : 1);  // one commit per issuer with stages in the tile
-      mbar_init(smem_u32(&tempty_bar[b]), 2 * kNatEpiWarps);
+      mbar_init(smem_u32(&tempty_bar[b]), 2 * NC::kEpiWarps);
     }
     mbar_init(smem_u32(drain_bar), 2);
-    if constexpr (kQ) requant_xchg_init(smem_out, kNatEpiWarps);
+    if constexpr (kQ) requant_xchg_init(smem_out, NC::kEpiWarps);
     *abort_flag = 0;
     *issue_turn = 0;
     fence_barrier_init();
@@ -580,116 +746,148 @@ __global__ void __launch_bounds__(kNatThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  const int num_tiles = args.num_pm * args.num_nb;
+  const int num_units = pair_num_units(args);
   uint32_t loads_issued = 0;
 
   if (warp == 0 || warp == 3) {
     // ----------------------------------------------------------- producers --
-    if (lane == 0) {
+    // Dense calls: lane 0 alone; M-grouped calls: the whole warp (warp-
+    // collective unit reads) with lane 0 issuing.
+    if (kGrouped || lane == 0) {
       const uint32_t me = warp == 0 ? 0u : 1u;
       const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
       const uint32_t empty0 = smem_u32(empty_bar), ring0 = smem_u32(ring);
-      uint32_t g = 0, stage = me, phase = 0;
+      uint32_t g = 0, stage = me, phase = 0;  // g: stages of this pair's MMA units so far
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        int pm, nb;
-        pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
-        const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
-        const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
+      UnitIds nxt = pair_unit_ids<kGrouped>(pair, args, lane);
+      for (int t = pair; t < num_units && ok; t += num_pairs) {
+        const UnitIds cur = nxt;
+        nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
+        const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+        for (int slot = 0; slot < u.nslots && ok; ++slot) {
+        const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
+        if (!ps.mma) continue;
+        const int arow = u.pm * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int brow = u.nb * kBNs + static_cast<int>(rank) * (kBNs / 2);
         for (int sl = 0; sl < nst; ++sl, ++g) {
           if ((g & 1u) != me) continue;
-          ok = mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, limit);
+          if (!kGrouped || lane == 0) {
+            ok = mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, limit);
+            if (ok) {
+              if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * NC::kStageBytes);
+              const uint32_t fb = leader_full + stage * 8u;
+              const uint32_t dst = ring0 + stage * NC::kStageBytes;
+              // K-major: 3-D maps {128, rows, K/128} (M-grouped B: 4-D with the
+              // expert last); MN-major: 2-D maps {rows, K} whose 256-row boxes
+              // stack the stage's two K blocks.
+              if (!kNT && args.a_mn)
+                tma_load_2d_pair(dst, &tmap_a, fb, arow, sl * NC::kKbPerStage * kBK);
+              else
+                tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * NC::kKbPerStage);
+              if constexpr (kGrouped)
+                tma_load_4d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, sl * NC::kKbPerStage, ps.g);
+              else if (!kNT && args.b_mn)
+                tma_load_2d_pair(dst + NC::kAStage, &tmap_b, fb, brow, sl * NC::kKbPerStage * kBK);
+              else
+                tma_load_3d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, sl * NC::kKbPerStage);
+              ++loads_issued;
+            }
+          }
+          if constexpr (kGrouped) ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kNatStageBytes);
-          const uint32_t fb = leader_full + stage * 8u;
-          const uint32_t dst = ring0 + stage * kNatStageBytes;
-          // K-major: 3-D maps {128, rows, K/128}; MN-major: 2-D maps {rows, K}
-          // whose 256-row boxes stack the stage's two K blocks.
-          if (!kNT && args.a_mn)
-            tma_load_2d_pair(dst, &tmap_a, fb, arow, sl * kNatKbPerStage * kBK);
-          else
-            tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * kNatKbPerStage);
-          if (!kNT && args.b_mn)
-            tma_load_2d_pair(dst + kNatAStageBytes, &tmap_b, fb, brow, sl * kNatKbPerStage * kBK);
-          else
-            tma_load_3d_pair(dst + kNatAStageBytes, &tmap_b, fb, 0, brow, sl * kNatKbPerStage);
-          ++loads_issued;
           stage += 2;
           if (stage >= static_cast<uint32_t>(S)) {
             stage -= S;
             phase ^= 1u;
           }
         }
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
     // ----------------------------------------------------------- MMA issue --
-    if (leader && lane == 0) {
+    if (leader && (kGrouped || lane == 0)) {
       const uint32_t me = static_cast<uint32_t>(warp - 1);
       const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
       const uint32_t ring0 = smem_u32(ring);
-      uint32_t g = 0, stage = me, sphase = 0, tl = 0;  // this issuer's stages: index parity me
+      // g: stages of this pair's MMA units so far (this issuer's: index parity
+      // me); tl: MMA units so far (the accumulator alternates with it).
+      uint32_t g = 0, stage = me, sphase = 0, tl = 0;
       const OperandTile at{static_cast<uint32_t>(args.a_mn), 128u}, bt{static_cast<uint32_t>(args.b_mn), 64u};
       const uint64_t afields = at.desc_fields(), bfields = bt.desc_fields();
       const uint32_t astep = at.kstep(), bstep = bt.kstep();
       const uint32_t idesc = args.idesc;
       bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
-        const uint32_t abuf = tl & 1u;
-        const uint32_t d = tmem_base + abuf * kBN;
+      UnitIds nxt = pair_unit_ids<kGrouped>(pair, args, lane);
+      for (int t = pair; t < num_units && ok; t += num_pairs) {
+        const UnitIds cur = nxt;
+        nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
+        const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+        for (int slot = 0; slot < u.nslots && ok; ++slot) {
+        if (!pair_slot<kGrouped>(u, slot, args).mma) continue;
+        const uint32_t abuf = tl % NC::kNumAcc;
+        const uint32_t d = tmem_base + abuf * kBNs;
         for (int sl = 0; sl < nst; ++sl, ++g) {
           if ((g & 1u) != me) continue;
-          ok = mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit);
-          if (ok && sl == 0)
-            ok = mbar_wait(smem_u32(&tempty_bar[abuf]), ((tl >> 1) & 1u) ^ 1u, abort_flag, status, limit);
-          // Wait for the other issuer to have handed the tensor pipe stage g - 1.
-          if (ok && *issue_turn != g) {
-            const uint64_t t0 = global_timer_ns();
-            for (uint32_t i = 0; *issue_turn != g; ++i) {
-              if ((i & 63u) == 63u && (*abort_flag || global_timer_ns() - t0 > limit)) {
-                if (!*abort_flag) {
-                  *abort_flag = 1;
-                  atomicOr(status, kStatusTimeout);
+          if (!kGrouped || lane == 0) {
+            ok = mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit);
+            if (ok && sl == 0)
+              ok = mbar_wait(smem_u32(&tempty_bar[abuf]), ((tl / NC::kNumAcc) & 1u) ^ 1u, abort_flag, status,
+                             limit);
+            // Wait for the other issuer to have handed the tensor pipe stage g - 1.
+            if (ok && *issue_turn != g) {
+              const uint64_t t0 = global_timer_ns();
+              for (uint32_t i = 0; *issue_turn != g; ++i) {
+                if ((i & 63u) == 63u && (*abort_flag || global_timer_ns() - t0 > limit)) {
+                  if (!*abort_flag) {
+                    *abort_flag = 1;
+                    atomicOr(status, kStatusTimeout);
+                  }
+                  ok = false;
+                  break;
                 }
-                ok = false;
-                break;
               }
             }
           }
+          if constexpr (kGrouped) ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
           if (!ok) break;
-          tc_fence_after();
-          const uint32_t base = ring0 + stage * kNatStageBytes;
+          if (!kGrouped || lane == 0) {
+            tc_fence_after();
+            const uint32_t base = ring0 + stage * NC::kStageBytes;
 #pragma unroll
-          for (int j = 0; j < kNatKbPerStage; ++j) {
-            const int kb = sl * kNatKbPerStage + j;
-            if (kb < args.num_kb) {
-              const uint32_t sfa = tmem_base + kAccCols + (stage * kNatKbPerStage + j) * kSfCols;
-              if constexpr (kNT) {
-                const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
-                const uint64_t bdesc = sw128_kmajor_desc(base + kNatAStageBytes + j * kBHalfBytes);
+            for (int j = 0; j < NC::kKbPerStage; ++j) {
+              const int kb = sl * NC::kKbPerStage + j;
+              if (kb < args.num_kb) {
+                const uint32_t sfa = tmem_base + NC::kAccCols + (stage * NC::kKbPerStage + j) * NC::kSfCols;
+                if constexpr (kNT) {
+                  const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
+                  const uint64_t bdesc = sw128_kmajor_desc(base + NC::kAStage + j * NC::kBHalf);
 #pragma unroll
-                for (int k = 0; k < kBK / 32; ++k)
-                  mma_e4m3_pair_scaled(d, adesc + 2u * k, bdesc + 2u * k, kIdescScaled, sfa, sfa + 4,
-                                       (kb > 0 || k > 0) ? 1u : 0u);
-              } else {
-                const uint64_t adesc = desc_at(afields, base + j * kABytes);
-                const uint64_t bdesc = desc_at(bfields, base + kNatAStageBytes + j * kBHalfBytes);
+                  for (int k = 0; k < kBK / 32; ++k)
+                    mma_e4m3_pair_scaled(d, adesc + 2u * k, bdesc + 2u * k, NC::kIdesc, sfa, sfa + 4,
+                                         (kb > 0 || k > 0) ? 1u : 0u);
+                } else {
+                  const uint64_t adesc = desc_at(afields, base + j * kABytes);
+                  const uint64_t bdesc = desc_at(bfields, base + NC::kAStage + j * NC::kBHalf);
 #pragma unroll
-                for (int k = 0; k < kBK / 32; ++k)
-                  mma_e4m3_pair_scaled(d, adesc + astep * k, bdesc + bstep * k, idesc, sfa, sfa + 4,
-                                       (kb > 0 || k > 0) ? 1u : 0u);
+                  for (int k = 0; k < kBK / 32; ++k)
+                    mma_e4m3_pair_scaled(d, adesc + astep * k, bdesc + bstep * k, idesc, sfa, sfa + 4,
+                                         (kb > 0 || k > 0) ? 1u : 0u);
+                }
               }
             }
+            mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
+            if (sl + 2 >= nst) mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
+            *issue_turn = g + 1;
           }
-          mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
-          if (sl + 2 >= nst) mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
-          *issue_turn = g + 1;
           stage += 2;
           if (stage >= static_cast<uint32_t>(S)) {
             stage -= S;
             sphase ^= 1u;
           }
+        }
+        ++tl;
         }
       }
     }
@@ -697,19 +895,29 @@ __global__ void __launch_bounds__(kNatThreads, 1)
   } else if (warp < kNatFirstEpiWarp) {
     // ------------------------------------------------------- scale writers --
     const uint32_t quad = warp & 3;
-    const uint32_t sf_row = tmem_base + ((quad * 32) << 16) + kAccCols;
+    const uint32_t sf_row = tmem_base + ((quad * 32) << 16) + NC::kAccCols;
     const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-      int pm, nb;
-      pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
-      const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
+    UnitIds nxt = pair_unit_ids<kGrouped>(pair, args, lane);
+    for (int t = pair; t < num_units && ok; t += num_pairs) {
+      const UnitIds cur = nxt;
+      nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
+      const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+      for (int slot = 0; slot < u.nslots && ok; ++slot) {
+      const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
+      if (!ps.mma) continue;
+      const int mb = min(u.pm * 2 + static_cast<int>(rank), args.num_mb - 1);
+      // The tile's B scale blocks: one for 128-column tiles, two (lo, hi) for
+      // 256-column tiles; a block past N repeats the last one (no output there).
+      const int sbb = kBNs == 256 ? u.nb * 2 : u.nb;
       const float* sa_p = args.sa + static_cast<int64_t>(mb) * args.ld_sa;
-      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.ld_sb;
+      const int nbs = (args.N + kBK - 1) / kBK;  // 128-row scale blocks of B (per expert)
+      const float* sb_p = args.sb + (static_cast<int64_t>(ps.g) * nbs + sbb) * args.ld_sb;
+      const float* sb_hi = sb_p + (sbb + 1 < nbs ? args.ld_sb : 0);
       for (int sl = 0; sl < nst; ++sl) {
-        const int kb0 = sl * kNatKbPerStage;
-        const bool two = kb0 + 1 < args.num_kb;
+        const int kb0 = sl * NC::kKbPerStage;
+        const bool two = NC::kKbPerStage == 2 && kb0 + 1 < args.num_kb;
         const uint32_t ea0 = ue8m0_word(__ldg(sa_p + kb0)), eb0 = ue8m0_word(__ldg(sb_p + kb0));
         const uint32_t ea1 = two ? ue8m0_word(__ldg(sa_p + kb0 + 1)) : ea0;
         const uint32_t eb1 = two ? ue8m0_word(__ldg(sb_p + kb0 + 1)) : eb0;
@@ -719,9 +927,13 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t col = sf_row + stage * kNatKbPerStage * kSfCols;
+        const uint32_t col = sf_row + stage * NC::kKbPerStage * NC::kSfCols;
         tmem_st8(col, ea0, ea0, ea0, ea0, eb0, eb0, eb0, eb0);
-        tmem_st8(col + kSfCols, ea1, ea1, ea1, ea1, eb1, eb1, eb1, eb1);
+        if constexpr (kBNs == 256) {
+          const uint32_t eh = ue8m0_word(__ldg(sb_hi + kb0));
+          tmem_st8(col + 8, eh, eh, eh, eh, eh, eh, eh, eh);
+        }
+        if constexpr (NC::kKbPerStage == 2) tmem_st8(col + NC::kSfCols, ea1, ea1, ea1, ea1, eb1, eb1, eb1, eb1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -730,6 +942,7 @@ __global__ void __launch_bounds__(kNatThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
+      }
       }
     }
     __syncwarp();
@@ -740,35 +953,110 @@ __global__ void __launch_bounds__(kNatThreads, 1)
     const int quad = warp & 3;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + part * 64;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty_bar), 0);
-    uint8_t* out_box = smem_out + ew * kBoxBytes * 2;
+    uint8_t* out_box = smem_out + ew * kBoxBytes * NC::kBoxes;
     bool stores_issued = false;
-    uint32_t tl = 0;
-    for (int t = pair; t < num_tiles; t += num_pairs, ++tl) {
-      int pm, nb;
-      pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
-      const uint32_t abuf = tl & 1u;
-      const bool w = mbar_wait(smem_u32(&tfull_bar[abuf]), (tl >> 1) & 1u, abort_flag, status, limit);
-      if (!__all_sync(0xFFFFFFFFu, w)) break;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld<32>(tmem_row + abuf * kBN, &r[0]);
-      tmem_ld<32>(tmem_row + abuf * kBN + 32, &r[32]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + abuf * 8u);
-      uint64_t acc[32];
+    uint32_t tl = 0;  // MMA units read so far (the accumulator alternates with it)
+    uint32_t xl = 0;  // tiles this CTA stored (the requantizing exchange's sequence)
+    bool ok = true;
+    for (int t = pair; t < num_units && ok; t += num_pairs) {
+      // No look-ahead here: the epilogue waits a whole tile for its accumulator,
+      // and the prefetched ids would cost registers that its loads need.
+      const PairUnit u = pair_unit<kGrouped>(t, args, pair_unit_ids<kGrouped>(t, args, lane));
+      for (int slot = 0; slot < u.nslots; ++slot) {
+      const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
+      const bool mine = ((ps.keep >> rank) & 1) != 0;
+      if constexpr (kBNs == 256) {
+        // bf16 output: round each 32-column load to bf16 before the next one,
+        // so that 32 registers, not 64, hold the slice.
+        uint32_t pk[32];
+        if (kGrouped && !ps.mma) {
+          if (ps.bad && mine && ew == 0 && lane == 0) atomicOr(status, kStatusBadGroup);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = f32x2(r[2 * j], r[2 * j + 1]);
-      const int row0 = pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
-      if constexpr (kQ) {
-        if (!requant_store_slice<kNatEpiWarps>(acc, row0 + lane < args.M, false, row0, args.M, args.N,
-                                               nb * kBN + part * 64, ew, lane, tl, smem_out, args.rq, &tmap_c,
-                                               requant_box(smem_out, kNatEpiWarps, ew), stores_issued, abort_flag,
-                                               status, limit))
-          break;
+          for (int j = 0; j < 32; ++j) pk[j] = 0u;
+        } else {
+          const uint32_t abuf = tl % NC::kNumAcc;
+          const bool w = mbar_wait(smem_u32(&tfull_bar[abuf]), (tl / NC::kNumAcc) & 1u, abort_flag, status, limit);
+          if (!__all_sync(0xFFFFFFFFu, w)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t r[32];
+            tmem_ld<32>(tmem_row + abuf * kBNs + q * 32, r);
+            tmem_wait_ld();
+            if (q == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + abuf * 8u);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[q * 16 + j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          }
+          ++tl;
+        }
+        if (!mine) continue;
+        const int row0 = u.pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
+        if constexpr (kGrouped) {
+          if (!ps.mma || __ldg(args.m_indices + row0 + lane) < 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pk[j] = 0u;
+          }
+        }
+        store_packed_rows(pk, tmap_c, args, out_box, row0, u.nb * kBNs + part * 64, lane, stores_issued);
+        continue;
+      }
+      uint64_t acc[32];
+      if (kGrouped && !ps.mma) {
+        // No MMAs: the kept rows are written as zeros; an id past the last
+        // expert is reported in the status word.
+        if (ps.bad && mine && ew == 0 && lane == 0) atomicOr(status, kStatusBadGroup);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0ull;
       } else {
-        store_tile_rows<64>(acc, tmap_c, args, out_box, row0, nb * kBN + part * 64, lane, stores_issued);
+        const uint32_t abuf = tl % NC::kNumAcc;
+        const bool w = mbar_wait(smem_u32(&tfull_bar[abuf]), (tl / NC::kNumAcc) & 1u, abort_flag, status, limit);
+        if (!__all_sync(0xFFFFFFFFu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld<32>(tmem_row + abuf * kBNs, &r[0]);
+        tmem_ld<32>(tmem_row + abuf * kBNs + 32, &r[32]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_addr(leader_tempty + abuf * 8u);
+        ++tl;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = f32x2(r[2 * j], r[2 * j + 1]);
+      }
+      if (!mine) continue;
+      const int row0 = u.pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32;
+      // M-grouped: rows of padding (id -1) are zeros.
+      bool zero_row = false;
+      if constexpr (kGrouped) {
+        zero_row = !ps.mma || __ldg(args.m_indices + row0 + lane) < 0;
+        if (zero_row) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] = 0ull;
+        }
+      }
+      if constexpr (kQ) {
+        if (!requant_store_slice<NC::kEpiWarps>(acc, row0 + lane < args.M && !zero_row, kGrouped, row0, args.M,
+                                                args.N, u.nb * kBNs + part * 64, ew, lane, xl, smem_out, args.rq,
+                                                &tmap_c, requant_box(smem_out, NC::kEpiWarps, ew), stores_issued,
+                                                abort_flag, status, limit)) {
+          ok = false;
+          break;
+        }
+        ++xl;
+      } else {
+        store_tile_rows<64, NC::kBoxes>(acc, tmap_c, args, out_box, row0, u.nb * kBNs + part * 64, lane,
+                                        stores_issued);
+      }
       }
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
@@ -817,27 +1105,44 @@ struct PairKind {
   int max_stages;
   int kb_per_stage;
 };
-template <bool kQ, bool kNT>
-PairKind pair_kind_t(bool scaled) {
+template <bool kQ, bool kNT, bool kGrouped, int kBNs>
+PairKind nat_kind_t() {
+  using NC = NatCfg<kBNs>;
+  return {reinterpret_cast<const void*>(&fp8_gemm_pair_scaled_kernel<kQ, kNT, kGrouped, kBNs>), NC::kThreads,
+          nat_out_bytes<kBNs>(kQ) + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, NC::kStageBytes,
+          kNatMaxStages, NC::kKbPerStage};
+}
+// The FP32-promotion pair kernel serves dense calls only (M-grouped calls with
+// FP32 scales take the kernels of gemm.cu): kGrouped kinds are block-scaled.
+template <bool kQ, bool kNT, bool kGrouped>
+PairKind pair_kind_t(bool scaled, bool wide) {
   using C = PCfg<kEpiCols, kQ>;
-  if (scaled)
-    return {reinterpret_cast<const void*>(&fp8_gemm_pair_scaled_kernel<kQ, kNT>), kNatThreads,
-            nat_out_bytes(kQ) + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16, kNatStageBytes, kNatMaxStages,
-            kNatKbPerStage};
+  if (kGrouped || scaled) {
+    if constexpr (!kQ && kNT) {
+      if (wide) return nat_kind_t<kQ, kNT, kGrouped, 256>();
+    }
+    return nat_kind_t<kQ, kNT, kGrouped, 128>();
+  }
   return {reinterpret_cast<const void*>(&fp8_gemm_pair_kernel<kEpiCols, kQ, kNT>), C::kThreads,
           C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
 }
-// variant = scaled + 2 * requant + 4 * NT layout
+// variant = scaled + 2 * requant + 4 * NT layout + 8 * M-grouped (always NT)
+//           + 16 * 256-column block-scaled tiles (bf16 output, NT)
+constexpr int kNumVariants = 32;
 PairKind pair_kind(int variant) {
-  const bool scaled = (variant & 1) != 0;
-  if (variant & 4) return (variant & 2) ? pair_kind_t<true, true>(scaled) : pair_kind_t<false, true>(scaled);
-  return (variant & 2) ? pair_kind_t<true, false>(scaled) : pair_kind_t<false, false>(scaled);
+  const bool scaled = (variant & 1) != 0, wide = (variant & 16) != 0;
+  if (variant & 8)
+    return (variant & 2) ? pair_kind_t<true, true, true>(scaled, wide) : pair_kind_t<false, true, true>(scaled, wide);
+  if (variant & 4)
+    return (variant & 2) ? pair_kind_t<true, true, false>(scaled, wide)
+                         : pair_kind_t<false, true, false>(scaled, wide);
+  return (variant & 2) ? pair_kind_t<true, false, false>(scaled, wide) : pair_kind_t<false, false, false>(scaled, wide);
 }
 
 // Largest number of co-resident CTA pairs of a kernel (cached per device).
 int max_active_pairs(int variant, size_t smem) {
   static std::mutex mu;
-  static int cache[64][8] = {};
+  static int cache[64][kNumVariants] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
@@ -866,7 +1171,7 @@ int max_active_pairs(int variant, size_t smem) {
 }
 
 bool set_pair_smem_attribute(int variant) {
-  static std::atomic<uint64_t> done[8] = {{0}, {0}, {0}, {0}, {0}, {0}, {0}, {0}};
+  static std::atomic<uint64_t> done[kNumVariants] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::atomic<uint64_t>& d = done[variant];
@@ -878,25 +1183,54 @@ bool set_pair_smem_attribute(int variant) {
   return true;
 }
 
-template <bool kQ, bool kNT>
-cudaError_t launch_pair(bool scaled, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, const CUtensorMap& ta,
-                        const CUtensorMap& tb, const CUtensorMap& tc, const PairArgsT<kQ>& a) {
-  if (scaled) return launch_kernel(fp8_gemm_pair_scaled_kernel<kQ, kNT>, grid, block, smem, stream, 2u, ta, tb, tc, a);
-  return launch_kernel(fp8_gemm_pair_kernel<kEpiCols, kQ, kNT>, grid, block, smem, stream, 2u, ta, tb, tc, a);
+template <bool kQ, bool kNT, bool kGrouped>
+cudaError_t launch_pair(bool scaled, bool wide, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                        const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        const PairArgsT<kQ, kGrouped>& a) {
+  if (kGrouped || scaled) {
+    if constexpr (!kQ && kNT) {
+      if (wide)
+        return launch_kernel(fp8_gemm_pair_scaled_kernel<kQ, kNT, kGrouped, 256>, grid, block, smem, stream, 2u, ta,
+                             tb, tc, a);
+    }
+    return launch_kernel(fp8_gemm_pair_scaled_kernel<kQ, kNT, kGrouped, 128>, grid, block, smem, stream, 2u, ta, tb,
+                         tc, a);
+  } else {
+    return launch_kernel(fp8_gemm_pair_kernel<kEpiCols, kQ, kNT>, grid, block, smem, stream, 2u, ta, tb, tc, a);
+  }
+}
+
+// The argument struct of an instantiation: the dense fields, plus the requant
+// output and/or the M-grouped fields.
+template <bool kQ, bool kG>
+PairArgsT<kQ, kG> make_args(const PairArgs& base, const GemmProblem& p) {
+  PairArgsT<kQ, kG> a{};
+  static_cast<PairArgs&>(a) = base;
+  if constexpr (kQ) a.rq = p.rq;
+  if constexpr (kG) {
+    a.m_indices = p.m_indices;
+    a.num_groups = p.num_groups;
+  }
+  return a;
 }
 
 }  // namespace
 
 int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
-  if (p.m_indices != nullptr || p.M <= kBM) return DG_ERR_UNSUPPORTED_SHAPE;
-  unsigned int* status = device_status_word();
-  if (!status) return DG_ERR_CUDA;
+  const bool grouped = p.m_indices != nullptr;
+  if (grouped ? (p.a_mn || p.b_mn) : p.M <= kBM) return DG_ERR_UNSUPPORTED_SHAPE;
   // The block-scaled kernel fills its scale columns uniformly, which needs one
   // A scale per 128 rows; per-row A scales take the FP32 promotion (exact too).
   const bool scaled = p.pow2_scales && !p.sa_per_row;
+  if (grouped && !scaled) return DG_ERR_UNSUPPORTED_SHAPE;
+  unsigned int* status = device_status_word();
+  if (!status) return DG_ERR_CUDA;
   const bool requant = p.rq.q != nullptr;
   const bool nt = !p.a_mn && !p.b_mn;
-  const int variant = (scaled ? 1 : 0) + (requant ? 2 : 0) + (nt ? 4 : 0);
+  // 256-column block-scaled tiles for bf16 output in the NT layout once N spans them.
+  const bool wide = scaled && !requant && nt && p.N > kBN;
+  const int bn = wide ? 2 * kBN : kBN;
+  const int variant = (scaled ? 1 : 0) + (requant ? 2 : 0) + (nt ? 4 : 0) + (grouped ? 8 : 0) + (wide ? 16 : 0);
   const PairKind kind = pair_kind(variant);
   PairArgs args{};
   args.c = static_cast<__nv_bfloat16*>(p.c);
@@ -912,10 +1246,10 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   args.ld_sb = static_cast<int>(p.ld_sb);
   args.a_mn = p.a_mn ? 1 : 0;
   args.b_mn = p.b_mn ? 1 : 0;
-  args.idesc = (scaled ? kIdescScaled : kIdesc) | idesc_majors(p.a_mn, p.b_mn);
+  args.idesc = (scaled ? (wide ? NatCfg<256>::kIdesc : NatCfg<128>::kIdesc) : kIdesc) | idesc_majors(p.a_mn, p.b_mn);
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_pm = static_cast<int>((p.M + 2 * kBM - 1) / (2 * kBM));
-  args.num_nb = static_cast<int>((p.N + kBN - 1) / kBN);
+  args.num_nb = static_cast<int>((p.N + bn - 1) / bn);
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
   const size_t budget = kMaxDynSmem - 1024 - kind.fixed_smem;
@@ -926,7 +1260,7 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   const size_t smem = 1024 + static_cast<size_t>(stages) * kind.stage_bytes + kind.fixed_smem;
   if (!set_pair_smem_attribute(variant)) return DG_ERR_CUDA;
 
-  const int64_t tiles = static_cast<int64_t>(args.num_pm) * args.num_nb;
+  const int64_t tiles = static_cast<int64_t>(args.num_pm) * args.num_nb * (grouped ? 2 : 1);
   int pairs = max_active_pairs(variant, smem);
   if (pairs <= 0) return DG_ERR_UNSUPPORTED_SHAPE;
   if (p.num_sms_cap > 0) pairs = std::min(pairs, p.num_sms_cap / 2);
@@ -951,7 +1285,26 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
                                    CU_TENSOR_MAP_SWIZZLE_64B))
       return DG_ERR_CUDA;
   }
-  if (kind.kb_per_stage == 1) {
+  if (grouped) {
+    // B as [G][N][K] (row stride K): the FP32-promotion kernel loads 2-D
+    // {K, N, G} boxes of 128 x 64 x 1; the block-scaled kernel {128, N, K/128,
+    // G} boxes of 128 x BN/2 x (K blocks per stage) x 1.
+    const uint64_t K = static_cast<uint64_t>(p.K), N = static_cast<uint64_t>(p.N);
+    const uint64_t G = static_cast<uint64_t>(p.num_groups);
+    if (!scaled) {
+      const uint64_t bdims[3] = {K, N, G};
+      const uint64_t bstr[2] = {K, K * N};
+      const uint32_t bbox[3] = {kBK, kBN / 2, 1};
+      if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true)) return DG_ERR_CUDA;
+    } else {
+      const uint64_t bdims[4] = {kBK, N, K / kBK, G};
+      const uint64_t bstr[3] = {K, kBK, K * N};
+      const uint32_t bbox[4] = {kBK, static_cast<uint32_t>(bn / 2), kbs, 1};
+      if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 4, bdims, bstr, bbox, true)) return DG_ERR_CUDA;
+    }
+  }
+  if (!scaled) {
+    // The FP32-promotion kernel: 2-D maps {K, rows}, one K block per box.
     const uint64_t adims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
     const uint64_t astr[1] = {static_cast<uint64_t>(p.ld_a)};
     const uint32_t abox[2] = {kBK, kBM};
@@ -959,18 +1312,19 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
     const uint64_t bstr[1] = {static_cast<uint64_t>(p.ld_b)};
     const uint32_t bbox[2] = {kBK, kBN / 2};
     if ((!p.a_mn && !encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, adims, astr, abox, true)) ||
-        (!p.b_mn && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, bdims, bstr, bbox, true)))
+        (!p.b_mn && !grouped && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, bdims, bstr, bbox, true)))
       return DG_ERR_CUDA;
   } else {
-    // [K/128][rows][128 bytes]: one box carries kb_per_stage K blocks.
+    // The block-scaled kernel: 3-D maps [K/128][rows][128 bytes], one box
+    // carries the stage's K blocks (B: BN/2 rows per CTA).
     const uint64_t adims[3] = {kBK, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K / kBK)};
     const uint64_t astr[2] = {static_cast<uint64_t>(p.ld_a), kBK};
     const uint32_t abox[3] = {kBK, kBM, kbs};
     const uint64_t bdims[3] = {kBK, static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K / kBK)};
     const uint64_t bstr[2] = {static_cast<uint64_t>(p.ld_b), kBK};
-    const uint32_t bbox[3] = {kBK, kBN / 2, kbs};
+    const uint32_t bbox[3] = {kBK, static_cast<uint32_t>(bn / 2), kbs};
     if ((!p.a_mn && !encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 3, adims, astr, abox, true)) ||
-        (!p.b_mn && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true)))
+        (!p.b_mn && !grouped && !encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 3, bdims, bstr, bbox, true)))
       return DG_ERR_CUDA;
   }
   if (requant) {
@@ -994,14 +1348,17 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   cudaError_t e;
   const dim3 grid(2 * pairs), block(kind.threads);
   if (requant) {
-    PairArgsQ qa;
-    static_cast<PairArgs&>(qa) = args;
-    qa.rq = p.rq;
-    e = nt ? launch_pair<true, true>(scaled, grid, block, smem, stream, ta, tb, tc, qa)
-           : launch_pair<true, false>(scaled, grid, block, smem, stream, ta, tb, tc, qa);
+    e = grouped ? launch_pair<true, true, true>(scaled, wide, grid, block, smem, stream, ta, tb, tc,
+                                                make_args<true, true>(args, p))
+        : nt    ? launch_pair<true, true, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc,
+                                                 make_args<true, false>(args, p))
+                : launch_pair<true, false, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc,
+                                                  make_args<true, false>(args, p));
   } else {
-    e = nt ? launch_pair<false, true>(scaled, grid, block, smem, stream, ta, tb, tc, args)
-           : launch_pair<false, false>(scaled, grid, block, smem, stream, ta, tb, tc, args);
+    e = grouped ? launch_pair<false, true, true>(scaled, wide, grid, block, smem, stream, ta, tb, tc,
+                                                 make_args<false, true>(args, p))
+        : nt    ? launch_pair<false, true, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc, args)
+                : launch_pair<false, false, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc, args);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -121,7 +121,8 @@ def test_grouped_matches_dense_bitwise(oracle_mod):
         assert torch.equal(cd.view(torch.int16), c[lo:hi].view(torch.int16))
 
 
-def test_expert_id_past_the_last_group_is_zeroed_and_reported(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_expert_id_past_the_last_group_is_zeroed_and_reported(oracle_mod, mode):
     """A 128-row block whose expert id equals num_groups reads no B or sb of
     that id, comes out as zeros, and sets DG_ERR_BAD_GROUP. B and sb are
     allocated for one expert more than num_groups, so that even a read of the
@@ -132,15 +133,16 @@ def test_expert_id_past_the_last_group_is_zeroed_and_reported(oracle_mod):
                             np.full(100, 1, np.int32), np.full(28, -1, np.int32)])
     a = synthetic.lognormal_rows((m_idx.size, k), seed=211)
     b = synthetic.lognormal_rows(((g + 1) * n, k), seed=212).reshape(g + 1, n, k)
-    qa, sa = oracle_mod.quantize(a)
-    qb, sb = _quantize_experts(oracle_mod, b)
+    qa, sa = oracle_mod.quantize(a, mode)
+    qb, sb = _quantize_experts(oracle_mod, b, mode)
     c = torch.full((m_idx.size, n), float("nan"), dtype=torch.bfloat16, device=dev)
-    qb_d, sb_d = to_dev(qb, dev), to_dev(sb, dev)
+    # Every device buffer stays referenced until the kernel has run.
+    qa_d, sa_d, qb_d, sb_d, mi_d = (to_dev(v, dev) for v in (qa, sa, qb, sb, m_idx))
     rc = bq.lib().dg_fp8_grouped_gemm_contiguous(
-        ctypes.c_void_p(c.data_ptr()), n, ctypes.c_void_p(to_dev(qa, dev).data_ptr()), k,
-        ctypes.c_void_p(to_dev(sa, dev).data_ptr()), ctypes.c_void_p(qb_d.data_ptr()),
-        ctypes.c_void_p(sb_d.data_ptr()), g, ctypes.c_void_p(to_dev(m_idx, dev).data_ptr()),
-        m_idx.size, n, k, 0, ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+        ctypes.c_void_p(c.data_ptr()), n, ctypes.c_void_p(qa_d.data_ptr()), k,
+        ctypes.c_void_p(sa_d.data_ptr()), ctypes.c_void_p(qb_d.data_ptr()),
+        ctypes.c_void_p(sb_d.data_ptr()), g, ctypes.c_void_p(mi_d.data_ptr()),
+        m_idx.size, n, k, mode, ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
     assert rc == bq.DG_OK
     assert bq.dg_get_device_status() == bq.DG_ERR_BAD_GROUP
     assert bq.dg_get_device_status() == bq.DG_OK          # taken and cleared
