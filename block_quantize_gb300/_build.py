@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libdgfp8.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["api.cpp", "quantize.cu", "gemm.cu", "gemm_smallm.cu", "gemm_pair.cu", "gemv.cu"]
-HEADERS = ["dg_device.cuh", "dg_encode.cuh", "dg_internal.h"]
+HEADERS = ["dg_device.cuh", "dg_encode.cuh", "dg_internal.h", "dg_pair.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -825,8 +825,9 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   // Decode shapes: one row streams B (gemv.cu); M <= 128, cluster split-K.
   if (!block_n_override() && gemv_supported(p)) return launch_gemv(p, stream);
   if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
-  // Dense M > 128 and every M-grouped call: CTA pairs (the grouped calls fall
-  // back to the 1-SM kernel below when fewer than two SMs are allowed).
+  // Dense M > 128 and M-grouped calls with power-of-two scales: CTA pairs (the
+  // grouped calls fall back to the 1-SM kernel below when fewer than two SMs
+  // are allowed).
   if (!block_n_override() && (p.m_indices != nullptr || p.M > kBM)) {
     const int r = launch_gemm_pair(p, stream);
     if (r != DG_ERR_UNSUPPORTED_SHAPE) return r;
