@@ -533,25 +533,28 @@ def small_records(dev, gen, stream, steps, warmup, hbm, ms_=None):
     return res
 
 
-def quantize_records(dev, gen, stream, r, cdim, steps, warmup, hbm, modes=(0, 1)):
-    """The 128x128 block quantizer on an FP32 [r, cdim] input rotated beyond L2:
-    read 4 B + write 1 B per element plus the scales."""
+def quantize_records(dev, gen, stream, shapes, steps, warmup, hbm, modes=(0, 1)):
+    """The 128x128 block quantizer on FP32 [r, cdim] inputs rotated beyond L2:
+    read 4 B + write 1 B per element plus the scales. Launches of a few
+    microseconds are replayed back to back from a CUDA graph (host launch cost
+    excluded), as a model step issues them."""
     import torch
     import block_quantize_gb300 as bq
-    copies = max(1, -(-3 * L2_BYTES // (r * cdim * 5)))
-    xs = [torch.randn((r, cdim), generator=gen, device=dev) for _ in range(copies)]
-    q = torch.empty((r, cdim), dtype=torch.uint8, device=dev)
-    s_ = torch.empty((-(-r // 128), -(-cdim // 128)), dtype=torch.float32, device=dev)
     res = []
-    for mode in modes:
-        fns = [lambda x=x: bq.dg_quantize_fp8_block(x, mode, q, s_) for x in xs]
-        ms = statistics.median(_time_each(stream, fns, steps, warmup))
-        _check_status(bq, "quantizer")
-        byts = r * cdim * 5 + s_.numel() * 4
-        res.append({"rows": r, "cols": cdim, "scales": "ue8m0" if mode else "fp32", "us": ms * 1e3,
-                    "gbs": byts / (ms * 1e-3) / 1e9, "bound": "hbm",
-                    "frac": byts / (ms * 1e-3) / 1e9 / hbm})
-    del xs
+    for r, cdim in shapes:
+        copies = max(1, -(-3 * L2_BYTES // (r * cdim * 5)))
+        xs = [torch.randn((r, cdim), generator=gen, device=dev) for _ in range(copies)]
+        q = torch.empty((r, cdim), dtype=torch.uint8, device=dev)
+        s_ = torch.empty((-(-r // 128), -(-cdim // 128)), dtype=torch.float32, device=dev)
+        for mode in modes:
+            fns = [lambda x=x: bq.dg_quantize_fp8_block(x, mode, q, s_) for x in xs]
+            ms = _time_graph(stream, fns * max(1, 24 // len(fns)), max(steps, 10))
+            _check_status(bq, "quantizer")
+            byts = r * cdim * 5 + s_.numel() * 4
+            res.append({"rows": r, "cols": cdim, "scales": "ue8m0" if mode else "fp32", "us": ms * 1e3,
+                        "gbs": byts / (ms * 1e-3) / 1e9, "bound": "hbm",
+                        "frac": byts / (ms * 1e-3) / 1e9 / hbm})
+        del xs
     return res
 
 
@@ -590,7 +593,8 @@ def _check_status(bq, what):
 def config_records(dev, gen, stream, fp8_peak, hbm):
     """Bounded timings of the metric's other workloads for the benchmark line."""
     steps, warmup = 10, 3
-    q = quantize_records(dev, gen, stream, *synthetic.QUANT_SHAPE, steps, warmup, hbm)
+    acts = sorted({(synthetic.LLM_M, k) for _, k in synthetic.LLM_NK})
+    q = quantize_records(dev, gen, stream, [synthetic.QUANT_SHAPE] + acts, steps, warmup, hbm)
     small = small_records(dev, gen, stream, steps, warmup, hbm)
     grouped = [grouped_record(dev, gen, stream, steps, warmup, fp8_peak, mode) for mode in (0, 1)]
     squares = []
@@ -599,10 +603,10 @@ def config_records(dev, gen, stream, fp8_peak, hbm):
                                 steps, warmup, fp8_peak)
     tiny = gemm_records(dev, gen, stream, [synthetic.TINY], 0, steps, warmup, fp8_peak)
     tiny[0]["bound"] = "latency"
-    return {"quantize_16384x7168": q, "small_m_decode": small, "grouped_moe": grouped,
+    return {"quantize": q, "small_m_decode": small, "grouped_moe": grouped,
             "square": squares, "tiny": tiny,
             "timing": f"CUDA events, median of {steps} launches after {warmup} warm-up launches; "
-                      "decode shapes replayed from a CUDA graph; inputs rotated beyond L2"}
+                      "quantizer and decode shapes replayed from a CUDA graph; inputs rotated beyond L2"}
 
 
 def run_aux(args):
@@ -634,7 +638,7 @@ def run_aux(args):
         out["results"] = small_records(dev, gen, stream, args.steps, args.warmup, hbm, ms_)
     elif kind == "quantize":
         r, cdim = (int(v) for v in (spec or "16384,7168").split(","))
-        out["results"] = quantize_records(dev, gen, stream, r, cdim, args.steps, args.warmup, hbm)
+        out["results"] = quantize_records(dev, gen, stream, [(r, cdim)], args.steps, args.warmup, hbm)
     elif kind == "quantize1x128":
         # Row-wise (1x128) activation quantizer, FP32 and bfloat16 inputs.
         r, cdim = (int(v) for v in (spec or "16384,7168").split(","))

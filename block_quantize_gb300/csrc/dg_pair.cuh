@@ -20,7 +20,8 @@ namespace {
 constexpr int kBM = 128;               // rows per CTA (256 per pair)
 constexpr int kBN = 128;               // columns per pair tile
 constexpr int kBK = 128;               // K block = scale block
-constexpr int kGroupPM = 8;            // raster group height in pair rows
+constexpr int kGroupPM = 8;            // raster group height in pair rows (A larger than L2 allows)
+constexpr int64_t kRasterABytes = 16ll << 20;  // A up to this size is swept whole per N band
 constexpr uint32_t kABytes = kBM * kBK;            // 16 KB
 constexpr uint32_t kBoxBytes = 32 * 32 * 2;        // one warp's 32 x 32 bf16 output box
 constexpr size_t kMaxDynSmem = 227 * 1024;
@@ -40,6 +41,7 @@ struct PairArgs {
   int num_mb;   // ceil(M / 128)
   int num_pm;   // ceil(M / 256)
   int num_nb;   // ceil(N / 128)
+  int group_pm; // raster group height in pair rows
   int num_stages;
   uint64_t wait_limit_ns;
 };
@@ -62,21 +64,20 @@ template <bool kQ, bool kG = false>
 using PairArgsT = std::conditional_t<kG, std::conditional_t<kQ, PairArgsQG, PairArgsG>,
                                      std::conditional_t<kQ, PairArgsQ, PairArgs>>;
 
-__device__ __forceinline__ void pair_tile_coords(int t, int num_pm, int num_nb, int& pm, int& nb) {
-  const int per_group = kGroupPM * num_nb;
+// Tile t of the raster: groups of group_pm pair rows, each swept over N with
+// the pair row fastest, so the pairs at work at once share a few B column
+// bands and one group's A rows. With the group spanning all of M (A small
+// enough to stay in L2) every B band is read from HBM once.
+__device__ __forceinline__ void pair_tile_coords(int t, int num_pm, int num_nb, int group_pm, int& pm, int& nb) {
+  const int per_group = group_pm * num_nb;
   const int grp = t / per_group;
-  const int first = grp * kGroupPM;
-  const int gm = min(kGroupPM, num_pm - first);
+  const int first = grp * group_pm;
+  const int gm = min(group_pm, num_pm - first);
   const int r = t - grp * per_group;
   pm = first + r % gm;
   nb = r / gm;
 }
 
-// One unit of a pair's persistent work: pair row pm (A rows [256 pm, +256)),
-// N tile nb, the expert whose B the MMAs read, which CTAs keep their 128 rows
-// (bit r: CTA r writes its rows; the other CTA's rows are discarded), and
-// whether the unit runs MMAs at all (a block of padding rows only, or of an
-// id past the last expert, is written as zeros without them).
 // A unit of a pair's persistent work: pair row pm (A rows [256 pm, +256)) and
 // N tile nb. Dense calls run one slot per unit. M-grouped calls (both 128-row
 // halves of a pair MMA multiply one B, so one expert) look up the experts g0,
@@ -110,7 +111,7 @@ __device__ __forceinline__ UnitIds pair_unit_ids(int t, const Args& a, int lane)
   if constexpr (kGrouped) {
     if (t < pair_num_units(a)) {
       int pm, nb;
-      pair_tile_coords(t, a.num_pm, a.num_nb, pm, nb);
+      pair_tile_coords(t, a.num_pm, a.num_nb, a.group_pm, pm, nb);
       const int4* ids = reinterpret_cast<const int4*>(a.m_indices);
       r.v0 = __ldg(ids + static_cast<int64_t>(2 * pm) * 32 + lane);
       if (2 * pm + 1 < a.num_mb) r.v1 = __ldg(ids + static_cast<int64_t>(2 * pm + 1) * 32 + lane);
@@ -122,7 +123,7 @@ __device__ __forceinline__ UnitIds pair_unit_ids(int t, const Args& a, int lane)
 template <bool kGrouped, class Args>
 __device__ __forceinline__ PairUnit pair_unit(int t, const Args& a, const UnitIds& ids) {
   PairUnit u;
-  pair_tile_coords(t, a.num_pm, a.num_nb, u.pm, u.nb);
+  pair_tile_coords(t, a.num_pm, a.num_nb, a.group_pm, u.pm, u.nb);
   u.g0 = u.g1 = 0;
   u.nslots = 1;
   if constexpr (kGrouped) {

@@ -101,7 +101,7 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
   uint32_t stage = 0, phase = 0, issued = 0;
   for (int t = pair; t < num_tiles; t += num_pairs) {
     int pm, nb;
-    pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+    pair_tile_coords(t, args.num_pm, args.num_nb, args.group_pm, pm, nb);
     const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
     const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
     for (int kb = 0; kb < args.num_kb; ++kb) {
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     // into L2 while the preceding grid finishes.
     if (pair < args.num_pm * args.num_nb) {
       int pm, nb;
-      pair_tile_coords(pair, args.num_pm, args.num_nb, pm, nb);
+      pair_tile_coords(pair, args.num_pm, args.num_nb, args.group_pm, pm, nb);
       const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
       const int n_pre = min(S, args.num_kb);
       for (int kb = 0; kb < n_pre; ++kb) {
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     bool ready = false;  // the full barrier of slot `it` is known to be complete
     for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
       int pm, nb;
-      pair_tile_coords(t, args.num_pm, args.num_nb, pm, nb);
+      pair_tile_coords(t, args.num_pm, args.num_nb, args.group_pm, pm, nb);
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
       // This thread's row's scales (rows past M read the last row's).
       const int arow = min(pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32 + lane, args.M - 1);
@@ -1018,6 +1018,9 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_pm = static_cast<int>((p.M + 2 * kBM - 1) / (2 * kBM));
   args.num_nb = static_cast<int>((p.N + bn - 1) / bn);
+  // All of M in one raster group when A fits comfortably in L2 (B is then
+  // read once), else groups of kGroupPM pair rows.
+  args.group_pm = (p.M * p.K <= kRasterABytes) ? std::max(args.num_pm, 1) : kGroupPM;
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
   const size_t budget = kMaxDynSmem - 1024 - kind.fixed_smem;

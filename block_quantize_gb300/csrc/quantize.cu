@@ -27,10 +27,12 @@
 // Two kernels share that arithmetic:
 //  * quantize_stream_kernel (16-byte-aligned input, row stride a multiple of 4
 //    floats): one persistent CTA per SM streams 128x128 FP32 blocks (64 KB)
-//    through a 3-stage TMA ring in shared memory guarded by mbarriers, so that
-//    ~190 KB per SM are in flight while earlier blocks are reduced and encoded
-//    from shared memory. Out-of-range rows and columns of edge blocks arrive
-//    as zeros (TMA fill), which leaves the block max unchanged.
+//    through a 3-stage TMA ring in shared memory guarded by mbarriers, two
+//    blocks ahead of the one being reduced and encoded (inputs of at most four
+//    blocks per SM: two single-stage CTAs per SM instead). Each block is copied
+//    from shared memory to registers once. Out-of-range rows and columns of
+//    edge blocks arrive as zeros (TMA fill), which leaves the block max
+//    unchanged.
 //  * quantize_kernel (any alignment): one CTA per block, the block held in
 //    registers between the two passes.
 //
@@ -251,24 +253,36 @@ __global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
   }
 }
 
-// Stages of the streaming ring: ~190 KB of input in flight per SM.
-template <bool kBf16>
+// Stages of the streaming ring (192 KB of shared memory, one CTA per SM).
+// A stage is refilled with the block kAhead ahead once its block has been
+// copied to registers; with kStages - 1 ahead the refill goes to the stage
+// freed an iteration earlier, which keeps two 64 KB FP32 blocks per SM in
+// flight (measured on GB300: 16384x7168 FP32 quantized at 6.9 TB/s against
+// 6.45 TB/s with three in flight).
+// kShort: one stage and two CTAs per SM (64 registers per thread), for inputs
+// of at most four blocks per SM. Each SM then encodes two blocks at once
+// instead of one after the other once the last loads land (measured: 4096x2048
+// FP32 in 8.2 us against 8.6 us).
+template <bool kBf16, bool kShort = false>
 struct StreamCfg {
   static constexpr int kElemBytes = kBf16 ? 2 : 4;
   static constexpr uint32_t kTileBytes = kBlock * kBlock * kElemBytes;
-  static constexpr int kStages = kBf16 ? 6 : 3;
+  static constexpr int kStages = kShort ? 1 : (kBf16 ? 6 : 3);
+  static constexpr int kAhead = kStages > 1 ? kStages - 1 : 1;
+  static constexpr int kCtasPerSm = kShort ? 2 : 1;
 };
 
 // kRowwise: one scale per row of the tile (1 x 128 blocks) instead of one per
 // tile; kBf16: bfloat16 input tiles, widened to FP32 exactly.
-template <bool kPow2, bool kRowwise, bool kBf16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kPow2, bool kRowwise, bool kBf16, bool kShort>
+__global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm)
     quantize_stream_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t rows, int64_t cols,
                            uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ scales,
                            int64_t blocks_per_row, int64_t nblocks, unsigned int* status,
                            uint64_t limit_ns) {
-  using SC = StreamCfg<kBf16>;
+  using SC = StreamCfg<kBf16, kShort>;
   constexpr int kStages = SC::kStages;
+  constexpr int kAhead = SC::kAhead;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmap_x);
-    for (int j = 0; j < kStages; ++j) issue(j);
+    for (int j = 0; j < kAhead; ++j) issue(j);
   }
 
   int64_t j = 0;
@@ -335,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t c0 = bj * kBlock + lane * 4;
     if constexpr (kRowwise) {
       __syncthreads();  // every thread has copied its part of the stage
-      if (threadIdx.x == 0) issue(j + kStages);
+      if (threadIdx.x == 0) issue(j + kAhead);
       // Row maxima; lane i then computes row i's scale and its reciprocal (one
       // division per warp instead of one per row), which the others read back.
       float my_amax = 0.f;
@@ -396,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
       if (lane == 0) warp_amax[warp] = __uint_as_float(wmax);
       __syncthreads();  // also: every thread has copied its part of the stage
-      // The stage is free again: refill it with the block kStages ahead.
-      if (threadIdx.x == 0) issue(j + kStages);
+      // Every thread has copied block j: the stage of block j + kAhead is free.
+      if (threadIdx.x == 0) issue(j + kAhead);
       float amax = warp_amax[0];
 #pragma unroll
       for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, warp_amax[w]);
@@ -432,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Launch the streaming kernel (16-byte-aligned x, row stride a multiple of 16
 // bytes); false if the tensor map cannot be made (the caller falls back).
-template <bool kPow2, bool kRowwise, bool kBf16>
+template <bool kPow2, bool kRowwise, bool kBf16, bool kShort = false>
 bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q, int64_t ld_q,
                    float* scales, cudaStream_t stream, cudaError_t& err) {
-  using SC = StreamCfg<kBf16>;
+  using SC = StreamCfg<kBf16, kShort>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   const int sms = device_sm_count(dev);
@@ -448,7 +462,7 @@ bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint
                          dims, strides, box, false))
     return false;
   const size_t smem = 1024 + SC::kStages * SC::kTileBytes + SC::kStages * 8 + kWarps * 4 + 16;
-  auto kernel = quantize_stream_kernel<kPow2, kRowwise, kBf16>;
+  auto kernel = quantize_stream_kernel<kPow2, kRowwise, kBf16, kShort>;
   static std::atomic<uint64_t> attr_set{0};
   if (!(attr_set.load() & (1ull << dev))) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -466,7 +480,7 @@ bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint
   const int64_t nbr = (rows + kBlock - 1) / kBlock;
   const int64_t nbc = (cols + kBlock - 1) / kBlock;
   const int64_t nblocks = nbr * nbc;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, sms));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, SC::kCtasPerSm * sms));
   err = launch_kernel(kernel, dim3(grid), dim3(kThreads), smem, stream, 0, tm, rows, cols, q, ld_q, scales, nbc,
                       nblocks, status, kDefaultWaitLimitNs);
   if (err != cudaSuccess) cudaGetLastError();
@@ -540,10 +554,17 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t 
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld_x % 4 == 0) &&
                    (reinterpret_cast<uintptr_t>(q) % 4 == 0) && (ld_q % 4 == 0);
   if (vec) {
+    int dev = 0;
+    const int sms = cudaGetDevice(&dev) == cudaSuccess ? device_sm_count(dev) : 0;
+    const bool short_input = sms > 0 && nblocks <= 4 * static_cast<int64_t>(sms);
     cudaError_t err = cudaSuccess;
-    const bool done = pow2_scales
-                          ? launch_stream<true, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
-                          : launch_stream<false, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    bool done;
+    if (short_input)
+      done = pow2_scales ? launch_stream<true, false, false, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, false, false, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    else
+      done = pow2_scales ? launch_stream<true, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
     if (done) return err;
   }
   const dim3 grid(static_cast<unsigned>(nblocks));
