@@ -364,6 +364,33 @@ DG_API int dg_fp8_k_grouped_gemm_tn(void* c, int64_t ld_c, const uint8_t* a, int
   if (dev_st != DG_OK) return dev_st;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint16_t* c16 = static_cast<uint16_t*>(c);
+  if (!dg::tile_width_forced()) {
+    // Every non-empty range in one launch on CTA pairs (FP32 scales, M > 128).
+    dg::GemmProblem p{};
+    p.c = c;
+    p.ld_c = ld_c;
+    p.a = a;
+    p.ld_a = ld_a;
+    p.sa = sa;
+    p.b = b;
+    p.ld_b = ld_b;
+    p.sb = sb;
+    p.num_groups = 1;
+    p.M = M;
+    p.N = N;
+    p.K = k_tot;
+    p.num_sms_cap = g_num_sms_cap.load();
+    p.pow2_scales = scale_mode == DG_SCALE_UE8M0;
+    p.a_mn = true;
+    p.b_mn = true;
+    p.ld_sa = p.ld_sb = k_tot / 128;
+    int r = dg::launch_gemm_pair_k_grouped(p, k_sizes, num_groups, st);
+    if (r != DG_ERR_UNSUPPORTED_SHAPE) {
+      for (int g = 0; g < num_groups && r == DG_OK; ++g)
+        if (k_sizes[g] == 0) r = zero_output(c16 + static_cast<int64_t>(g) * M * ld_c, ld_c, M, N, st);
+      return r;
+    }
+  }
   int64_t k_off = 0;
   for (int g = 0; g < num_groups; ++g) {
     void* cg = c16 + static_cast<int64_t>(g) * M * ld_c;

@@ -91,12 +91,22 @@ struct GemmProblem {
 // Returns a dg_status value.
 int launch_gemm(const GemmProblem& p, cudaStream_t stream);
 
+// DG_GEMM_BLOCK_N set: every GEMM takes the 1-SM kernel with that tile width.
+bool tile_width_forced();
+
 // Writes v into n consecutive floats of device memory.
 cudaError_t launch_fill_f32(float* dst, int64_t n, float v, cudaStream_t stream);
 
 // Dense GEMMs with M > 128 on CTA pairs (gemm_pair.cu); DG_ERR_UNSUPPORTED_SHAPE
 // when the problem or the launch limits do not allow a pair kernel.
 int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream);
+
+// K-grouped TN GEMM with FP32 scales on CTA pairs, every non-empty K range in
+// one launch: C_g [M][ld_c] at c + g * M * ld_c is A^T B over the K rows of
+// range g (k_sizes[g] rows each, in order, multiples of 128; p.K is their
+// sum). Ranges with K = 0 are left untouched (the caller zero-fills them).
+// DG_ERR_UNSUPPORTED_SHAPE when the call needs the per-range path.
+int launch_gemm_pair_k_grouped(const GemmProblem& p, const int64_t* k_sizes, int num_groups, cudaStream_t stream);
 
 // Dense GEMMs with M <= 128 use the cluster split-K kernel (gemm_smallm.cu).
 bool small_m_supported(int64_t M, const void* m_indices);

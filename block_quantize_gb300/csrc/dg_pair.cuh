@@ -63,6 +63,19 @@ struct PairArgsQG : PairArgsQ, PairGroups {};
 template <bool kQ, bool kG = false>
 using PairArgsT = std::conditional_t<kG, std::conditional_t<kQ, PairArgsQG, PairArgsG>,
                                      std::conditional_t<kQ, PairArgsQ, PairArgs>>;
+// K-grouped calls (one output matrix per range of K, the MoE weight gradient
+// C_g = A_g^T B_g): the ranges with K > 0, in K order. Unit t of such a launch
+// is tile t % T of range t / T (T = num_pm * num_nb tiles per range).
+constexpr int kMaxKGroups = 256;
+struct KGroups {
+  int num_kg;                // ranges with K > 0
+  int kb_lo[kMaxKGroups];    // first K block of the range
+  int kb_n[kMaxKGroups];     // K blocks of the range (> 0)
+  int g_out[kMaxKGroups];    // output matrix of the range
+};
+struct PairArgsKG : PairArgs, KGroups {};
+template <bool kQ, bool kKG>
+using PairArgsF = std::conditional_t<kKG, PairArgsKG, PairArgsT<kQ>>;
 
 // Tile t of the raster: groups of group_pm pair rows, each swept over N with
 // the pair row fastest, so the pairs at work at once share a few B column
@@ -165,10 +178,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 // chunk c of row r at chunk c ^ ((r / 2) % 4)) -> TMA stores, clipped at M.
 // A box that crosses column N is written element by element instead: the
 // swizzled store clips N only to whole 16-byte chunks.
-template <int EC, int kBoxes = EC / 32>
+// k3D: C is [G][M][ld_c] with a 3-D map {N, M, G}; the rows go to matrix g.
+template <int EC, int kBoxes = EC / 32, bool k3D = false>
 __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], const CUtensorMap& tmap_c,
                                                 const PairArgs& args, uint8_t* out_box, int row0, int col0,
-                                                int lane, bool& stores_issued) {
+                                                int lane, bool& stores_issued, int g = 0) {
   if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last tile's stores have read the boxes
   __syncwarp();
 #pragma unroll
@@ -181,7 +195,7 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
     if (bcol + 32 > args.N) {
       const int row = row0 + lane;
       if (row < args.M && bcol < args.N) {
-        __nv_bfloat16* crow = args.c + static_cast<int64_t>(row) * args.ld_c;
+        __nv_bfloat16* crow = args.c + (static_cast<int64_t>(g) * args.M + row) * args.ld_c;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float2 v = f32x2_split(acc[h * 16 + j]);
@@ -207,7 +221,10 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && row0 < args.M) {
-      tma_store_2d(&tmap_c, smem_u32(box), bcol, row0);
+      if constexpr (k3D)
+        tma_store_3d(&tmap_c, smem_u32(box), bcol, row0, g);
+      else
+        tma_store_2d(&tmap_c, smem_u32(box), bcol, row0);
       bulk_commit();
       stores_issued = true;
     }

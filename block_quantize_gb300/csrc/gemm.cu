@@ -803,6 +803,8 @@ bool encode_tensor_map_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, cons
 
 int device_sm_count(int dev) { return device_info(dev).num_sms; }
 
+bool tile_width_forced() { return block_n_override() != 0; }
+
 unsigned int* device_status_word() {
   static unsigned int* ptrs[64] = {nullptr};
   static std::mutex mu;

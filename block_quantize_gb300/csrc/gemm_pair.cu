@@ -81,6 +81,38 @@ struct PCfg {
 };
 constexpr int kEpiCols = 64;
 
+// One unit of the FP32-promotion kernel: pair tile (pm, nb) over K blocks
+// [kb0, kb0 + nkb), written to output matrix g (K-grouped calls; else g = 0
+// and the whole K).
+struct KUnit {
+  int pm, nb, kb0, nkb, g;
+};
+template <bool kKG, class Args>
+__device__ __forceinline__ int pair_units(const Args& a) {
+  if constexpr (kKG)
+    return a.num_kg * a.num_pm * a.num_nb;
+  else
+    return a.num_pm * a.num_nb;
+}
+template <bool kKG, class Args>
+__device__ __forceinline__ KUnit pair_kunit(int t, const Args& a) {
+  KUnit u;
+  if constexpr (kKG) {
+    const int per = a.num_pm * a.num_nb;
+    const int i = t / per;
+    pair_tile_coords(t - i * per, a.num_pm, a.num_nb, a.group_pm, u.pm, u.nb);
+    u.kb0 = a.kb_lo[i];
+    u.nkb = a.kb_n[i];
+    u.g = a.g_out[i];
+  } else {
+    pair_tile_coords(t, a.num_pm, a.num_nb, a.group_pm, u.pm, u.nb);
+    u.kb0 = 0;
+    u.nkb = a.num_kb;
+    u.g = 0;
+  }
+  return u;
+}
+
 // TMA producer of both pair kernels, run by one thread per CTA. CTA r loads
 // A rows [256 pm + 128 r, +128) and B rows [128 nb + 64 r, +64) of each K
 // block into ring stage it % S; both CTAs' bytes count on the even CTA's
@@ -88,23 +120,22 @@ constexpr int kEpiCols = 64;
 // SM sub-partition with busy warps and each TMA issue blocks it for a few
 // hundred cycles, so stage and phase are running counters. Returns the number
 // of stages it filled.
-template <bool kNT>
+template <bool kNT, bool kKG = false, class Args>
 __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                                                  const PairArgs& args, uint32_t ring0, uint64_t* full_bar,
+                                                  const Args& args, uint32_t ring0, uint64_t* full_bar,
                                                   uint64_t* empty_bar, uint32_t rank, int pair, int num_pairs,
                                                   volatile int* abort_flag, unsigned int* status) {
   const int S = args.num_stages;
   const bool leader = rank == 0;
   const uint32_t leader_full = mapa_shared(smem_u32(full_bar), 0);
   const uint32_t empty0 = smem_u32(empty_bar);
-  const int num_tiles = args.num_pm * args.num_nb;
+  const int num_units = pair_units<kKG>(args);
   uint32_t stage = 0, phase = 0, issued = 0;
-  for (int t = pair; t < num_tiles; t += num_pairs) {
-    int pm, nb;
-    pair_tile_coords(t, args.num_pm, args.num_nb, args.group_pm, pm, nb);
-    const int arow = pm * (2 * kBM) + static_cast<int>(rank) * kBM;
-    const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
-    for (int kb = 0; kb < args.num_kb; ++kb) {
+  for (int t = pair; t < num_units; t += num_pairs) {
+    const KUnit u = pair_kunit<kKG>(t, args);
+    const int arow = u.pm * (2 * kBM) + static_cast<int>(rank) * kBM;
+    const int brow = u.nb * kBN + static_cast<int>(rank) * (kBN / 2);
+    for (int kb = u.kb0; kb < u.kb0 + u.nkb; ++kb) {
       if (!mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, args.wait_limit_ns)) return issued;
       if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
       const uint32_t fb = leader_full + stage * 8u;
@@ -131,12 +162,14 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
 // kNT: both operands K-major (the NT layout). Its instantiation keeps layout
 // handling out of the TMA and MMA issue loops, where runtime branches on the
 // layout and runtime descriptors cost ~10 % (measured); other layouts take
-// the runtime path.
-template <int EC, bool kQ, bool kNT>
+// the runtime path. kKG: a K-grouped call (bf16 output, any layout), its units
+// spread over all ranges' tiles in one launch.
+template <int EC, bool kQ, bool kNT, bool kKG = false>
 __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
-                         const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ> args) {
+                         const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ PairArgsF<kQ, kKG> args) {
+  static_assert(!(kKG && kQ), "K-grouped calls write bf16");
   using C = PCfg<EC, kQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -180,12 +213,11 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     tma_prefetch_desc(&tmap_c);
     // The first stages' B half-tiles of this CTA's first tile start streaming
     // into L2 while the preceding grid finishes.
-    if (pair < args.num_pm * args.num_nb) {
-      int pm, nb;
-      pair_tile_coords(pair, args.num_pm, args.num_nb, args.group_pm, pm, nb);
-      const int brow = nb * kBN + static_cast<int>(rank) * (kBN / 2);
-      const int n_pre = min(S, args.num_kb);
-      for (int kb = 0; kb < n_pre; ++kb) {
+    if (pair < pair_units<kKG>(args)) {
+      const KUnit u = pair_kunit<kKG>(pair, args);
+      const int brow = u.nb * kBN + static_cast<int>(rank) * (kBN / 2);
+      const int n_pre = min(S, u.nkb);
+      for (int kb = u.kb0; kb < u.kb0 + n_pre; ++kb) {
         if (!kNT && args.b_mn)
           tma_prefetch_2d(&tmap_b, brow, kb * kBK);
         else
@@ -201,14 +233,14 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  const int num_tiles = args.num_pm * args.num_nb;
+  const int num_tiles = pair_units<kKG>(args);
   uint32_t loads_issued = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0)
-      loads_issued = pair_producer<kNT>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
-                                   num_pairs, abort_flag, status);
+      loads_issued = pair_producer<kNT, kKG>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
+                                             num_pairs, abort_flag, status);
     __syncwarp();
   } else if (warp <= kIssuers) {
     // ----------------------------------------------------------- MMA issue --
@@ -216,8 +248,14 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     // its stages and buffers advance by two (S is even, four buffers).
     if (leader && lane == 0) {
       const uint32_t me = static_cast<uint32_t>(warp - 1);
-      const int my_tiles = num_tiles > pair ? (num_tiles - 1 - pair) / num_pairs + 1 : 0;
-      const uint32_t total = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(args.num_kb);
+      uint32_t total;
+      if constexpr (kKG) {
+        total = 0;
+        for (int t = pair; t < num_tiles; t += num_pairs) total += static_cast<uint32_t>(pair_kunit<true>(t, args).nkb);
+      } else {
+        const int my_tiles = num_tiles > pair ? (num_tiles - 1 - pair) / num_pairs + 1 : 0;
+        total = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(args.num_kb);
+      }
       const uint32_t full0 = smem_u32(full_bar), empty0 = smem_u32(empty_bar);
       const uint32_t tfull0 = smem_u32(tfull_bar), tempty0 = smem_u32(tempty_bar);
       const uint32_t ring0 = smem_u32(ring);
@@ -275,20 +313,20 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
     bool ok = true;
     bool ready = false;  // the full barrier of slot `it` is known to be complete
     for (int t = pair; t < num_tiles && ok; t += num_pairs, ++tl) {
-      int pm, nb;
-      pair_tile_coords(t, args.num_pm, args.num_nb, args.group_pm, pm, nb);
+      const KUnit u = pair_kunit<kKG>(t, args);
+      const int pm = u.pm, nb = u.nb;
       const int mb = min(pm * 2 + static_cast<int>(rank), args.num_mb - 1);
       // This thread's row's scales (rows past M read the last row's).
       const int arow = min(pm * (2 * kBM) + static_cast<int>(rank) * kBM + quad * 32 + lane, args.M - 1);
-      const float* sa_p = args.sa + static_cast<int64_t>(args.sa_per_row ? arow : mb) * args.ld_sa;
-      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.ld_sb;
+      const float* sa_p = args.sa + static_cast<int64_t>(args.sa_per_row ? arow : mb) * args.ld_sa + u.kb0;
+      const float* sb_p = args.sb + static_cast<int64_t>(nb) * args.ld_sb + u.kb0;
       uint64_t acc[EC / 2];  // FP32 accumulators, two columns per register pair
 #pragma unroll
       for (int j = 0; j < EC / 2; ++j) acc[j] = 0ull;
       // Scales of K blocks kb + 1 (a1, b1) and kb + 2 (a2, b2) are loaded ahead
       // and multiplied only when used: a product right after its loads would
       // stall every K block on the load latency (measured: ~200 cycles).
-      const int num_kb = args.num_kb;
+      const int num_kb = u.nkb;
       float s = __ldg(sa_p) * __ldg(sb_p);
       float a1 = num_kb > 1 ? __ldg(sa_p + 1) : 0.f, b1 = num_kb > 1 ? __ldg(sb_p + 1) : 0.f;
       float a2 = num_kb > 2 ? __ldg(sa_p + 2) : 0.f, b2 = num_kb > 2 ? __ldg(sb_p + 2) : 0.f;
@@ -335,7 +373,8 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
           break;
         }
       } else {
-        store_tile_rows<EC>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane, stores_issued);
+        store_tile_rows<EC, EC / 32, kKG>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane,
+                                          stores_issued, u.g);
       }
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
@@ -895,9 +934,16 @@ PairKind pair_kind_t(bool scaled, bool wide) {
           C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
 }
 // variant = scaled + 2 * requant + 4 * NT layout + 8 * M-grouped (always NT)
-//           + 16 * 256-column block-scaled tiles (bf16 output, NT)
-constexpr int kNumVariants = 32;
+//           + 16 * 256-column block-scaled tiles (bf16 output, NT);
+// kKGroupedVariant: the FP32-promotion kernel over K ranges (bf16 output).
+constexpr int kKGroupedVariant = 32;
+constexpr int kNumVariants = 33;
 PairKind pair_kind(int variant) {
+  if (variant == kKGroupedVariant) {
+    using C = PCfg<kEpiCols, false>;
+    return {reinterpret_cast<const void*>(&fp8_gemm_pair_kernel<kEpiCols, false, false, true>), C::kThreads,
+            C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
+  }
   const bool scaled = (variant & 1) != 0, wide = (variant & 16) != 0;
   if (variant & 8)
     return (variant & 2) ? pair_kind_t<true, true, true>(scaled, wide) : pair_kind_t<false, true, true>(scaled, wide);
@@ -1131,6 +1177,99 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
         : nt    ? launch_pair<false, true, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc, args)
                 : launch_pair<false, false, false>(scaled, wide, grid, block, smem, stream, ta, tb, tc, args);
   }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  return DG_OK;
+}
+
+int launch_gemm_pair_k_grouped(const GemmProblem& p, const int64_t* k_sizes, int num_groups, cudaStream_t stream) {
+  if (p.pow2_scales || p.rq.q || p.m_indices || p.sa_per_row || !p.a_mn || !p.b_mn || p.M <= kBM)
+    return DG_ERR_UNSUPPORTED_SHAPE;
+  PairArgsKG args{};
+  int nkg = 0;
+  int64_t kb = 0, max_k = 0;
+  for (int g = 0; g < num_groups; ++g) {
+    if (k_sizes[g] > 0) {
+      if (nkg == kMaxKGroups) return DG_ERR_UNSUPPORTED_SHAPE;
+      args.kb_lo[nkg] = static_cast<int>(kb);
+      args.kb_n[nkg] = static_cast<int>(k_sizes[g] / kBK);
+      args.g_out[nkg] = g;
+      ++nkg;
+      max_k = std::max(max_k, k_sizes[g]);
+    }
+    kb += k_sizes[g] / kBK;
+  }
+  if (nkg == 0) return DG_OK;
+  args.num_kg = nkg;
+  unsigned int* status = device_status_word();
+  if (!status) return DG_ERR_CUDA;
+  args.c = static_cast<__nv_bfloat16*>(p.c);
+  args.ld_c = p.ld_c;
+  args.sa = p.sa;
+  args.sa_per_row = 0;
+  args.sb = p.sb;
+  args.status = status;
+  args.M = static_cast<int>(p.M);
+  args.N = static_cast<int>(p.N);
+  args.num_kb = static_cast<int>(kb);
+  args.ld_sa = static_cast<int>(p.ld_sa);
+  args.ld_sb = static_cast<int>(p.ld_sb);
+  args.a_mn = 1;
+  args.b_mn = 1;
+  args.idesc = kIdesc | idesc_majors(true, true);
+  args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
+  args.num_pm = static_cast<int>((p.M + 2 * kBM - 1) / (2 * kBM));
+  args.num_nb = static_cast<int>((p.N + kBN - 1) / kBN);
+  args.group_pm = (p.M * max_k <= kRasterABytes) ? std::max(args.num_pm, 1) : kGroupPM;
+  args.wait_limit_ns = kDefaultWaitLimitNs;
+
+  const PairKind kind = pair_kind(kKGroupedVariant);
+  const size_t budget = kMaxDynSmem - 1024 - kind.fixed_smem;
+  int stages = std::min<int>(kind.max_stages, static_cast<int>(budget / kind.stage_bytes));
+  stages = stages / 2 * 2;
+  if (stages < 4) return DG_ERR_UNSUPPORTED_SHAPE;
+  args.num_stages = stages;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * kind.stage_bytes + kind.fixed_smem;
+  if (!set_pair_smem_attribute(kKGroupedVariant)) return DG_ERR_CUDA;
+  const int64_t units = static_cast<int64_t>(args.num_pm) * args.num_nb * nkg;
+  int pairs = max_active_pairs(kKGroupedVariant, smem);
+  if (pairs <= 0) return DG_ERR_UNSUPPORTED_SHAPE;
+  if (p.num_sms_cap > 0) pairs = std::min(pairs, p.num_sms_cap / 2);
+  pairs = static_cast<int>(std::min<int64_t>(pairs, units));
+  if (pairs < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+
+  CUtensorMap ta, tb, tc;
+  {
+    // A as [K_tot][ld_a]: 128 (M) x 128 (K) boxes, 128-byte swizzle.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(kb * kBK)};
+    const uint64_t str[1] = {static_cast<uint64_t>(p.ld_a)};
+    const uint32_t box[2] = {kBM, kBK};
+    if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, str, box, true)) return DG_ERR_CUDA;
+  }
+  {
+    // B as [K_tot][ld_b]: 64 (N) x 128 (K) boxes, 64-byte swizzle.
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(kb * kBK)};
+    const uint64_t str[1] = {static_cast<uint64_t>(p.ld_b)};
+    const uint32_t box[2] = {kBN / 2, kBK};
+    if (!encode_tensor_map_swizzle(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, str, box,
+                                   CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
+  }
+  {
+    // C as bf16 [G][M][ld_c]: 32 x 32 x 1 boxes, 64-byte swizzle; rows past M
+    // of one matrix are clipped instead of reaching the next.
+    const uint64_t dims[3] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M),
+                              static_cast<uint64_t>(num_groups)};
+    const uint64_t str[2] = {static_cast<uint64_t>(p.ld_c) * 2, static_cast<uint64_t>(p.ld_c) * 2 * p.M};
+    const uint32_t box[3] = {32, 32, 1};
+    if (!encode_tensor_map_swizzle(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.c, 3, dims, str, box,
+                                   CU_TENSOR_MAP_SWIZZLE_64B))
+      return DG_ERR_CUDA;
+  }
+  const cudaError_t e = launch_kernel(fp8_gemm_pair_kernel<kEpiCols, false, false, true>, dim3(2 * pairs),
+                                      dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;

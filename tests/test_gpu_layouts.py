@@ -167,6 +167,28 @@ def test_k_grouped_small_m_exact(oracle_mod):
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
+def test_k_grouped_many_ranges_exact(oracle_mod):
+    """Twenty ranges of 0-384 rows (empty ones among them) in one launch: the
+    units of consecutive ranges share the pairs, and a pair row (M = 384) and a
+    column tile (N = 320) cross the matrix edges of every output."""
+    rng = np.random.default_rng(7)
+    sizes = [int(v) * 128 for v in rng.integers(0, 4, 20)]
+    sizes[0], sizes[-1] = 0, 256
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 384, 320, sizes, exact=True, seed=37)
+    ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
+    assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
+
+
+def test_k_grouped_more_ranges_than_one_launch_holds_exact(oracle_mod):
+    """300 non-empty ranges: past the 256 a single launch carries, the ranges
+    run one after another."""
+    sizes = [128] * 300
+    sizes[5] = 0
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 256, 128, sizes, exact=True, seed=39)
+    ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
+    assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
+
+
 def test_k_grouped_moe_weight_gradient_sampled(oracle_mod):
     """8 experts, token counts padded to 128 (the MoE layout's group sizes),
     M = 2048 hidden x N = 1408 intermediate: the shape of a weight gradient."""
