@@ -6,7 +6,7 @@
 // rows the work is streaming B from HBM, so the kernel is shaped for bytes in
 // flight on as many SMs as possible:
 //   * a thread-block cluster of `split` CTAs shares one BN-column tile of C
-//     (BN = 256 when M <= 64, else 128); CTA r of the cluster streams B over
+//     (BN = 128, 192 or 256, see plan_and_run); CTA r of the cluster streams B over
 //     its own contiguous K range through a deep TMA ring, issues the MMAs and
 //     promotes the partials in registers exactly like the large-M kernel.
 //     TMA boxes of 128-byte rows stream at ~40 GB/s per SM and, over all SMs,
@@ -644,7 +644,7 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
   // (mostly waiting for the slowest peer; measured, then swept). Time = max(whole-GPU stream of B,
   // the slowest cluster's K range per tile + its reductions).
   const double sm_bytes_per_us = 4.5e4;
-  const double gpu_bytes_per_us = (BN == 256) ? 5.4e6 : 4.8e6;
+  const double gpu_bytes_per_us = (BN == 256) ? 5.4e6 : (BN == 192) ? 5.2e6 : 4.8e6;
   const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (split > args.num_kb || (BN / 8) / split < 1) break;
@@ -730,7 +730,11 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
   return DG_OK;
 }
 
-// 256-column tiles (fewer, larger TMA boxes) when the partial tile fits.
+// The tile width with the least modelled time: 256 columns (fewer, larger TMA
+// boxes), 128, or -- bf16 output with K-major B -- 192, whose tile count often
+// fills the SMs where 256 leaves a third of them idle (24576 columns: 128
+// tiles of 192 against 96 of 256; 7168 columns: 38 tiles of 192 x a K split of
+// 4 = 152 CTAs).
 template <bool kQ>
 int plan_and_run(const GemmProblem& p, cudaStream_t stream, int sms, const SmallArgs& args) {
   if (!set_smem_attribute<256, kQ>() || !set_smem_attribute<128, kQ>()) return DG_ERR_CUDA;
@@ -739,6 +743,17 @@ int plan_and_run(const GemmProblem& p, cudaStream_t stream, int sms, const Small
   Plan p256, p128;
   const bool ok256 = plan_small_m<256, kQ>(p, sms, a256, s256, p256);
   const bool ok128 = plan_small_m<128, kQ>(p, sms, a128, s128, p128);
+  if constexpr (!kQ) {
+    if (!p.b_mn) {
+      if (!set_smem_attribute<192, kQ>()) return DG_ERR_CUDA;
+      SmallArgs a192 = args;
+      size_t s192 = 0;
+      Plan p192;
+      if (plan_small_m<192, kQ>(p, sms, a192, s192, p192) && (!ok256 || p192.cost < p256.cost) &&
+          (!ok128 || p192.cost < p128.cost))
+        return run_small_m<192, kQ>(p, stream, a192, s192, p192);
+    }
+  }
   if (ok256 && (!ok128 || p256.cost <= p128.cost)) return run_small_m<256, kQ>(p, stream, a256, s256, p256);
   if (ok128) return run_small_m<128, kQ>(p, stream, a128, s128, p128);
   return DG_ERR_UNSUPPORTED_SHAPE;
