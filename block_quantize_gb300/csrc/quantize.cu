@@ -37,9 +37,12 @@
 //    registers between the two passes.
 //
 // The row-wise variant (blocks of 1 x 128, per-token activation scales, pzsr.cn
-// page §3.1; FP32 or bfloat16 input) gives each warp a contiguous run of
-// (row, 128-column segment) pairs: lane l holds columns [4l, 4l + 4) of a
-// segment, four segments are loaded before any is reduced, the segment max is
+// page §3.1; FP32 or bfloat16 input) runs on quantize_stream_kernel too when
+// the input is 16-byte aligned: each warp's eight rows of a tile get one warp
+// reduction each, and lane i forms row i's scale and reciprocal for the warp.
+// Other inputs take quantize_1x128_kernel, which gives each warp a contiguous
+// run of (row, 128-column segment) pairs: lane l holds columns [4l, 4l + 4) of
+// a segment, four segments are loaded before any is reduced, the segment max is
 // one warp reduction, and the same encode4 arithmetic produces the codes.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
   }
 }
 
-// Stages of the streaming ring (192 KB of shared memory, one CTA per SM).
+// Stages of the streaming ring (FP32: 192 KB of shared memory, one CTA per SM).
 // A stage is refilled with the block kAhead ahead once its block has been
 // copied to registers; with kStages - 1 ahead the refill goes to the stage
 // freed an iteration earlier, which keeps two 64 KB FP32 blocks per SM in
@@ -263,13 +266,17 @@ __global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
 // of at most four blocks per SM. Each SM then encodes two blocks at once
 // instead of one after the other once the last loads land (measured: 4096x2048
 // FP32 in 8.2 us against 8.6 us).
+// bfloat16 tiles (32 KB) carry half the bytes of FP32 ones for the same
+// arithmetic, so that kernel is bound by instruction latency with one CTA's
+// 16 warps per SM: it runs two CTAs of three stages per SM (measured:
+// 16384x7168 row-wise in 73.5 us against 92.5 us with one CTA of six stages).
 template <bool kBf16, bool kShort = false>
 struct StreamCfg {
   static constexpr int kElemBytes = kBf16 ? 2 : 4;
   static constexpr uint32_t kTileBytes = kBlock * kBlock * kElemBytes;
-  static constexpr int kStages = kShort ? 1 : (kBf16 ? 6 : 3);
+  static constexpr int kStages = kBf16 ? 3 : (kShort ? 1 : 3);
   static constexpr int kAhead = kStages > 1 ? kStages - 1 : 1;
-  static constexpr int kCtasPerSm = kShort ? 2 : 1;
+  static constexpr int kCtasPerSm = (kShort || kBf16) ? 2 : 1;
 };
 
 // kRowwise: one scale per row of the tile (1 x 128 blocks) instead of one per
@@ -309,30 +316,35 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
   pdl_wait();
   pdl_trigger();
 
-  int64_t issued = 0;  // thread 0: blocks whose load was issued (in order)
-  auto issue = [&](int64_t j) {  // load this CTA's j-th block into stage j % kStages
-    const int64_t blk = blockIdx.x + j * gridDim.x;
+  // Block indices fit in 32 bits (the host checks nblocks); 32-bit arithmetic
+  // keeps 64-bit division out of the per-block path.
+  const int bpr = static_cast<int>(blocks_per_row);
+  int issued = 0;  // thread 0: blocks whose load was issued (in order)
+  auto issue = [&](int j) {  // load this CTA's j-th block into stage j % kStages
+    const int64_t blk = blockIdx.x + static_cast<int64_t>(j) * gridDim.x;
     if (blk >= nblocks) return;
     issued = j + 1;
-    const int64_t bi = blk / blocks_per_row, bj = blk - bi * blocks_per_row;
-    const int st = static_cast<int>(j % kStages);
+    const int b32 = static_cast<int>(blk);
+    const int bi = b32 / bpr, bj = b32 - bi * bpr;
+    const int st = j % kStages;
     const uint32_t fb = smem_u32(&full[st]);
     mbar_arrive_expect_tx(fb, SC::kTileBytes);
-    tma_load_2d(smem_u32(stage_data + st * SC::kTileBytes), &tmap_x, fb, static_cast<int32_t>(bj * kBlock),
-                static_cast<int32_t>(bi * kBlock));
+    tma_load_2d(smem_u32(stage_data + st * SC::kTileBytes), &tmap_x, fb, bj * kBlock, bi * kBlock);
   };
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmap_x);
     for (int j = 0; j < kAhead; ++j) issue(j);
   }
 
-  int64_t j = 0;
+  // This CTA's block (bi, bj), stage and phase advance as running counters.
+  int bi = static_cast<int>(blockIdx.x) / bpr, bj = static_cast<int>(blockIdx.x) - bi * bpr;
+  const int gdiv = static_cast<int>(gridDim.x) / bpr, gmod = static_cast<int>(gridDim.x) - gdiv * bpr;
+  int st = 0;
+  uint32_t ph = 0;
+  int j = 0;
   for (int64_t blk = blockIdx.x; blk < nblocks; blk += gridDim.x, ++j) {
-    const int st = static_cast<int>(j % kStages);
-    const bool ok = mbar_wait(smem_u32(&full[st]), static_cast<uint32_t>((j / kStages) & 1), abort_flag,
-                              status, limit_ns);
+    const bool ok = mbar_wait(smem_u32(&full[st]), ph, abort_flag, status, limit_ns);
     if (__syncthreads_or(!ok)) break;
-    const int64_t bi = blk / blocks_per_row, bj = blk - bi * blocks_per_row;
     float4 v[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -345,8 +357,8 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
         v[i] = reinterpret_cast<const float4*>(stage_data + st * SC::kTileBytes + tr * kBlock * 4)[lane];
       }
     }
-    const int64_t r0 = bi * kBlock + warp * kRowsPerWarp;
-    const int64_t c0 = bj * kBlock + lane * 4;
+    const int64_t r0 = static_cast<int64_t>(bi) * kBlock + warp * kRowsPerWarp;
+    const int64_t c0 = static_cast<int64_t>(bj) * kBlock + lane * 4;
     if constexpr (kRowwise) {
       __syncthreads();  // every thread has copied its part of the stage
       if (threadIdx.x == 0) issue(j + kAhead);
@@ -365,40 +377,47 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
       if constexpr (kPow2) my_s = pow2_round_up(my_s);
       const float my_r = 1.0f / my_s;
       if (lane < kRowsPerWarp && r0 + lane < rows) scales[(r0 + lane) * blocks_per_row + bj] = my_s;
+      // Rows whose scale is subnormal are always divided (bit i: row i).
+      const uint32_t tiny = kPow2 ? 0u : __ballot_sync(0xFFFFFFFFu, lane < kRowsPerWarp && my_s < 0x1p-126f);
       // Every row's codes first (independent work that can interleave), then
       // the rare exact divisions, then the stores.
       uint32_t code[kRowsPerWarp];
-      float s_row[kRowsPerWarp];
-      uint32_t bad = 0;
+      uint32_t bad = tiny;
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i) {
-        const float s = __shfl_sync(0xFFFFFFFFu, my_s, i);
         const float r = __shfl_sync(0xFFFFFFFFu, my_r, i);
-        s_row[i] = s;
         if constexpr (kPow2) {
-          code[i] = encode4<1>(v[i], s, r);
+          code[i] = encode4<1>(v[i], 1.0f, r);  // power-of-two scale: v * r is exact
         } else {
           bool ok;
           code[i] = encode4_bracketed(v[i], r, ok);
-          bad |= (ok && s >= 0x1p-126f ? 0u : 1u) << i;  // a subnormal scale is always divided
+          bad |= (ok ? 0u : 1u) << i;
         }
       }
-      if (!kPow2 && bad != 0u) {
+      if (!kPow2 && __any_sync(0xFFFFFFFFu, bad != 0u)) {
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i)
-          if ((bad >> i) & 1u) code[i] = encode4<2>(v[i], s_row[i], 0.0f);
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          const float s = __shfl_sync(0xFFFFFFFFu, my_s, i);
+          if ((bad >> i) & 1u) code[i] = encode4<2>(v[i], s, 0.0f);
+        }
       }
+      if (r0 + kRowsPerWarp <= rows && c0 + 3 < cols) {  // all of this thread's groups are inside
+        uint8_t* out = q + r0 * ld_q + c0;
 #pragma unroll
-      for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int64_t row = r0 + i;
-        if (row < rows) {
-          uint8_t* out = q + row * ld_q + c0;
-          if (c0 + 3 < cols) {
-            __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
-          } else {
+        for (int i = 0; i < kRowsPerWarp; ++i, out += ld_q) __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
+      } else {
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-              if (c0 + t < cols) out[t] = static_cast<uint8_t>((code[i] >> (8 * t)) & 0xFFu);
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+          const int64_t row = r0 + i;
+          if (row < rows) {
+            uint8_t* out = q + row * ld_q + c0;
+            if (c0 + 3 < cols) {
+              __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 4; ++t)
+                if (c0 + t < cols) out[t] = static_cast<uint8_t>((code[i] >> (8 * t)) & 0xFFu);
+            }
           }
         }
       }
@@ -429,11 +448,21 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
       }
       __syncthreads();  // warp_amax is rewritten by the next block
     }
+    if (++st == kStages) {
+      st = 0;
+      ph ^= 1u;
+    }
+    bi += gdiv;
+    bj += gmod;
+    if (bj >= bpr) {
+      bj -= bpr;
+      ++bi;
+    }
   }
   // After a timeout, loads still in flight (blocks j .. issued-1) must land
   // before the CTA exits; each gets a bounded wait on its own phase.
   if (threadIdx.x == 0 && *abort_flag) {
-    for (int64_t jj = j; jj < issued; ++jj) {
+    for (int jj = j; jj < issued; ++jj) {
       const uint32_t bar = smem_u32(&full[jj % kStages]);
       const uint32_t par = static_cast<uint32_t>((jj / kStages) & 1);
       const uint64_t t0 = global_timer_ns();
@@ -480,6 +509,7 @@ bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint
   const int64_t nbr = (rows + kBlock - 1) / kBlock;
   const int64_t nbc = (cols + kBlock - 1) / kBlock;
   const int64_t nblocks = nbr * nbc;
+  if (nblocks > 0x7FFFFFFFll) return false;  // block indices are 32-bit in the kernel
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(nblocks, SC::kCtasPerSm * sms));
   err = launch_kernel(kernel, dim3(grid), dim3(kThreads), smem, stream, 0, tm, rows, cols, q, ld_q, scales, nbc,
                       nblocks, status, kDefaultWaitLimitNs);
