@@ -609,7 +609,83 @@ def config_records(dev, gen, stream, fp8_peak, hbm):
                       "quantizer and decode shapes replayed from a CUDA graph; inputs rotated beyond L2"}
 
 
+def cpu_baseline_records():
+    """The oracle (plain C, float64 accumulation, OpenMP over output rows) timed
+    on the host cores over every config: the CPU baseline reported beside the
+    GPU figures, not a target. Config 1 and the 16384x7168 quantizer also run on
+    one core. Weights are quantized outside the timed GEMMs, as on the GPU;
+    activations are quantized inside them. The 16384^3 square runs 512 evenly
+    spaced rows of C and is extrapolated to the whole output (labelled)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    res = []
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        out = fn()
+        return time.perf_counter() - t0, out
+
+    def gemm(config, a, b, threads, rows=None):
+        oracle.set_num_threads(threads)
+        qb, sb = oracle.quantize(b)
+        t, _ = timed(lambda: oracle.gemm_nt(*oracle.quantize(a), qb, sb, rows=rows, want_e=False))
+        m, k = a.shape
+        n = b.shape[0]
+        done = m if rows is None else len(rows)
+        flops = 2.0 * done * n * k
+        rec = {"config": config, "M": m, "N": n, "K": k, "threads": threads, "seconds": t,
+               "gflops": flops / t / 1e9}
+        if rows is not None:
+            rec["rows_computed"] = done
+            rec["seconds_extrapolated_full"] = t * m / done
+        res.append(rec)
+
+    try:
+        m, n, k = synthetic.TINY
+        a, b = synthetic.normal((m, k), synthetic.seed_for(1, 0)), synthetic.normal((n, k), synthetic.seed_for(1, 1))
+        for th in (1, cores):
+            gemm("1 tiny", a, b, th)
+        x = synthetic.normal(synthetic.QUANT_SHAPE, synthetic.seed_for(3, 9))
+        for th in (1, cores):
+            oracle.set_num_threads(th)
+            t, _ = timed(lambda: oracle.quantize(x))
+            res.append({"config": "3 quantizer", "rows": x.shape[0], "cols": x.shape[1], "threads": th,
+                        "seconds": t, "gbs": x.size * 5 / t / 1e9})
+        del x
+        for idx, (m, n, k) in enumerate(shapes()):
+            sd = synthetic.seed_for(2, idx)
+            gemm("2 LLM projection", synthetic.lognormal_rows((m, k), sd), synthetic.lognormal_rows((n, k), sd + 500),
+                 cores)
+        for n, k in synthetic.SMALL_NK:
+            b = synthetic.normal((n, k), synthetic.seed_for(3, n))
+            for m in synthetic.SMALL_M:
+                gemm("3 decode", synthetic.normal((m, k), synthetic.seed_for(3, m)), b, cores)
+        a, b, m_idx, sizes = synthetic.moe_inputs()
+        oracle.set_num_threads(cores)
+        qbs = [oracle.quantize(b[g]) for g in range(b.shape[0])]
+        qb, sb = np.stack([q for q, _ in qbs]), np.stack([s_ for _, s_ in qbs])
+        t, _ = timed(lambda: oracle.grouped_gemm_contiguous(*oracle.quantize(a), qb, sb, m_idx, want_e=False))
+        res.append({"config": "4 MoE grouped", "M_tot": a.shape[0], "N": b.shape[1], "K": b.shape[2], "G": b.shape[0],
+                    "threads": cores, "seconds": t,
+                    "gflops_executed": 2.0 * a.shape[0] * b.shape[1] * b.shape[2] / t / 1e9})
+        del a, b, qb, sb, qbs
+        for sq in synthetic.SQUARES:
+            a = synthetic.normal((sq, sq), synthetic.seed_for(5, sq))
+            b = synthetic.normal((sq, sq), synthetic.seed_for(5, sq + 1))
+            rows = None if sq <= 8192 else np.linspace(0, sq - 1, 512).astype(np.int64)
+            gemm("5 square", a, b, cores, rows=rows)
+            del a, b
+    finally:
+        oracle.set_num_threads(cores)
+    return {"cores": cores, "kind": "oracle", "results": res}
+
+
 def run_aux(args):
+    if args.workload == "cpu_baseline":  # the oracle alone: host cores, no GPU
+        print(json.dumps({"workload": args.workload, **cpu_baseline_records()}), flush=True)
+        return 0
     import torch
     import block_quantize_gb300 as bq
     dev = torch.device("cuda", 0)
@@ -761,7 +837,7 @@ def main():
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
                         "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K] | "
-                        "requant[:M,N,K[:variant]] | layouts[:M,N,K] | kgrouped  "
+                        "requant[:M,N,K[:variant]] | layouts[:M,N,K] | kgrouped | cpu_baseline  "
                         "(the others print per-kernel numbers for profiling)")
     args = p.parse_args()
     if args.steps is None:
