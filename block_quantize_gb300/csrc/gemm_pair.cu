@@ -15,9 +15,10 @@
 // 128x128 partial and TMEM holds four of them. Each CTA also holds half as
 // many FP32 accumulators in registers, and each SM stages only its half of B.
 //
-//   * CTA r of a pair loads A rows [256 pm + 128 r, +128) and B rows
-//     [128 nb + 64 r, +64) of every K block with TMA; both loads count on the
-//     even CTA's `full` barrier, which the even CTA arms for both CTAs' bytes;
+//   * CTA r of a pair loads A rows [256 pm + 128 r, +128) (warp 0) and B rows
+//     [128 nb + 64 r, +64) (the last warp) of every K block with TMA; all loads
+//     count on the even CTA's `full` barrier, which the even CTA arms for both
+//     CTAs' bytes;
 //   * warps 1 and 2 of the even CTA take turns issuing the four MMAs (K = 32)
 //     of a K block into TMEM buffer it % 4 of both CTAs; each commit arrives on
 //     the stage's `empty` barrier and the buffer's `tfull` barrier in both
@@ -70,7 +71,8 @@ struct PCfg {
   static constexpr int kEpiPerQuad = kBN / kEpiCols;  // warps per TMEM lane quadrant
   static constexpr int kEpiWarps = 4 * kEpiPerQuad;
   static constexpr int kFirstEpiWarp = 1 + kIssuers;
-  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+  static constexpr int kBProducer = kFirstEpiWarp + kEpiWarps;  // the last warp loads B
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps + 1);
   // bf16 output: staging boxes for the TMA stores; E4M3 output: the slices'
   // maxima exchange (codes are stored straight from registers).
   static constexpr uint32_t kOutBytes =
@@ -113,14 +115,16 @@ __device__ __forceinline__ KUnit pair_kunit(int t, const Args& a) {
   return u;
 }
 
-// TMA producer of both pair kernels, run by one thread per CTA. CTA r loads
-// A rows [256 pm + 128 r, +128) and B rows [128 nb + 64 r, +64) of each K
-// block into ring stage it % S; both CTAs' bytes count on the even CTA's
-// `full` barrier, which the even CTA arms for the pair. The thread shares its
-// SM sub-partition with busy warps and each TMA issue blocks it for a few
-// hundred cycles, so stage and phase are running counters. Returns the number
-// of stages it filled.
-template <bool kNT, bool kKG = false, class Args>
+// TMA producer of the FP32-promotion pair kernel. CTA r loads A rows
+// [256 pm + 128 r, +128) and B rows [128 nb + 64 r, +64) of each K block into
+// ring stage it % S; both CTAs' bytes count on the even CTA's `full` barrier,
+// which the even CTA's A producer arms for the pair (a B load that lands
+// before the arm only takes the barrier's byte count below zero for the
+// phase). Each TMA issue blocks its thread for a few hundred cycles, about
+// what the tensor core spends on a K block, so one thread per operand issues
+// (kPart 1: A and the arm, kPart 2: B). Stage and phase are running counters.
+// Returns the number of stages it filled.
+template <bool kNT, bool kKG = false, int kPart = 0, class Args>
 __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                                                   const Args& args, uint32_t ring0, uint64_t* full_bar,
                                                   uint64_t* empty_bar, uint32_t rank, int pair, int num_pairs,
@@ -137,18 +141,22 @@ __device__ __forceinline__ uint32_t pair_producer(const CUtensorMap& tmap_a, con
     const int brow = u.nb * kBN + static_cast<int>(rank) * (kBN / 2);
     for (int kb = u.kb0; kb < u.kb0 + u.nkb; ++kb) {
       if (!mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, args.wait_limit_ns)) return issued;
-      if (leader) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
+      if (leader && kPart != 2) mbar_arrive_expect_tx(smem_u32(&full_bar[stage]), 2u * kStageBytes);
       const uint32_t fb = leader_full + stage * 8u;
       const uint32_t dst = ring0 + stage * kStageBytes;
       // K-major maps are {K, rows}; MN-major maps {rows, K} (the tile's K rows hold 128 or 64 bytes).
-      if (!kNT && args.a_mn)
-        tma_load_2d_pair(dst, &tmap_a, fb, arow, kb * kBK);
-      else
-        tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
-      if (!kNT && args.b_mn)
-        tma_load_2d_pair(dst + kABytes, &tmap_b, fb, brow, kb * kBK);
-      else
-        tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
+      if (kPart != 2) {
+        if (!kNT && args.a_mn)
+          tma_load_2d_pair(dst, &tmap_a, fb, arow, kb * kBK);
+        else
+          tma_load_2d_pair(dst, &tmap_a, fb, kb * kBK, arow);
+      }
+      if (kPart != 1) {
+        if (!kNT && args.b_mn)
+          tma_load_2d_pair(dst + kABytes, &tmap_b, fb, brow, kb * kBK);
+        else
+          tma_load_2d_pair(dst + kABytes, &tmap_b, fb, kb * kBK, brow);
+      }
       ++issued;
       if (++stage == static_cast<uint32_t>(S)) {
         stage = 0;
@@ -239,8 +247,14 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0)
-      loads_issued = pair_producer<kNT, kKG>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
-                                             num_pairs, abort_flag, status);
+      loads_issued = pair_producer<kNT, kKG, 1>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
+                                                num_pairs, abort_flag, status);
+    __syncwarp();
+  } else if (warp == C::kBProducer) {
+    // ---------------------------------------------------------- B producer --
+    if (lane == 0)
+      pair_producer<kNT, kKG, 2>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair, num_pairs,
+                                 abort_flag, status);
     __syncwarp();
   } else if (warp <= kIssuers) {
     // ----------------------------------------------------------- MMA issue --
