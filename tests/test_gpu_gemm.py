@@ -117,6 +117,19 @@ def test_small_m_shapes(oracle_mod, m, nk):
     _check(oracle_mod, qa, sa, qb, sb, rows=rows, what=f"{m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m", [16, 64])
+def test_decode_192_column_tiles_with_ragged_last_tile(oracle_mod, m):
+    """N = 24512 with K = 1536: 128 tiles of 192 columns fill the SMs better
+    than 96 of 256, and the last 192-column tile is cut at N; every column of
+    the last tiles is checked, with ld_c > N so that no store may cross it."""
+    n, k = 24512, 1536
+    qa, sa, qb, sb = _operands(oracle_mod, m, n, k, seed=1000 + m)
+    c, cbuf = _run(qa, sa, qb, sb, ldc_pad=40)
+    assert torch.isnan(cbuf[:, n:].float()).all()
+    ref, mag = oracle_mod.gemm_nt(qa, sa, qb, sb)
+    assert_within_bound(c, ref, mag, f"{m}x{n}x{k}")
+
+
 @pytest.mark.parametrize("size", synthetic.SQUARES)
 @pytest.mark.parametrize("mode", [0, 1])
 def test_square_shapes(oracle_mod, size, mode):

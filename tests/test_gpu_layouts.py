@@ -179,6 +179,24 @@ def test_k_grouped_many_ranges_exact(oracle_mod):
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
+def test_k_grouped_padded_output_rows_untouched(oracle_mod):
+    """One launch writing C [G][M][ld_c] with ld_c > N: every value of the
+    padding columns stays as it was (the 3-D output map clips at N and at M)."""
+    sizes = [256, 0, 128, 384]
+    m, n, ld = 300, 200, 232
+    k_tot = sum(sizes)
+    qa, sa, qb, sb = _exact_logical(m, n, k_tot, 43)
+    a_st, b_st = np.ascontiguousarray(qa.T), np.ascontiguousarray(qb.T)
+    dev = device()
+    c_full = torch.full((len(sizes), m, ld), float("nan"), dtype=torch.bfloat16, device=dev)
+    c = c_full[:, :, :n]
+    bq.dg_fp8_k_grouped_gemm_tn(c, _padded(a_st, dev), _padded(b_st, dev), to_dev(sa, dev), to_dev(sb, dev), sizes)
+    assert bq.dg_get_device_status() == bq.DG_OK
+    ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
+    assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
+    assert torch.isnan(c_full[:, :, n:].float()).all()
+
+
 def test_k_grouped_more_ranges_than_one_launch_holds_exact(oracle_mod):
     """300 non-empty ranges: past the 256 a single launch carries, the ranges
     run one after another."""
