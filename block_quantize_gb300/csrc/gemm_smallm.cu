@@ -267,8 +267,10 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
   size_t off = static_cast<size_t>(S) * (args.a_stage_bytes + C::kBTileBytes);
   const size_t a_read_end = static_cast<size_t>(S - 1) * args.a_stage_bytes + kATileBytes;
   if (a_read_end > off) off = a_read_end;  // an MMA reads 128 A rows from its stage
+  // The partial tile parked for the cluster's reduction (split >= 2 only: a
+  // CTA that reduces alone stores from registers and gets no buffer).
   float* part = reinterpret_cast<float*>(smem + off);
-  off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  if (args.split > 1) off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
   // Requantized output (kQ): the block-max exchange.
   uint8_t* rq_xchg = nullptr;
   uint32_t* rq_pmax = nullptr;  // [2][128][kNBlk]
@@ -609,6 +611,8 @@ int max_active_clusters(int split, size_t smem) {
 struct Plan {
   int split = 0;
   int clusters = 0;
+  int stages = 0;
+  size_t smem = 0;
   double cost = 1e300;
 };
 
@@ -619,24 +623,35 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
   using C = SCfg<BN>;
   args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
   const uint32_t stage_bytes = args.a_stage_bytes + C::kBTileBytes;
-  const size_t part_bytes = (static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float) + 15) / 16 * 16 +
-                            (kQ ? C::kRqBytes : 0);
   const size_t bar_bytes = (2 * kMaxStages + 2 * C::kNumPBuf + 3) * sizeof(uint64_t) + 32;
-  if (part_bytes + bar_bytes + 1024 >= kMaxDynSmem) return false;
-  const size_t budget = kMaxDynSmem - 1024 - part_bytes - bar_bytes;
   auto ring_bytes = [&](int st) {
     return std::max<size_t>(static_cast<size_t>(st) * stage_bytes,
                             static_cast<size_t>(st - 1) * args.a_stage_bytes + kATileBytes);
   };
-  int stages = std::min<int>(kMaxStages, static_cast<int>(budget / stage_bytes));
-  while (stages > C::kIssuers && ring_bytes(stages) > budget) --stages;
-  stages = stages / C::kIssuers * C::kIssuers;  // whole stage sets per issuer
-  if (stages < std::max(C::kIssuers, 4) || ring_bytes(stages) > budget) return false;
-  args.num_stages = stages;
-  size_t smem = 1024 + ring_bytes(stages) + part_bytes + bar_bytes;
-  smem = std::max<size_t>(smem, kMinSmemPerCta);
-  if (smem > kMaxDynSmem) return false;
-  smem_out = smem;
+  // Stages and shared memory without (split = 1) and with (split >= 2) the
+  // parked partial tile: at M = 128 the partial takes ~100 KB, which a CTA
+  // that reduces alone spends on stages instead.
+  auto layout = [&](bool with_part, int& stages_out, size_t& smem_o) {
+    const size_t part_bytes =
+        (with_part ? (static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float) + 15) / 16 * 16 : 0) +
+        (kQ ? C::kRqBytes : 0);
+    if (part_bytes + bar_bytes + 1024 >= kMaxDynSmem) return false;
+    const size_t budget = kMaxDynSmem - 1024 - part_bytes - bar_bytes;
+    int stages = std::min<int>(kMaxStages, static_cast<int>(budget / stage_bytes));
+    while (stages > C::kIssuers && ring_bytes(stages) > budget) --stages;
+    stages = stages / C::kIssuers * C::kIssuers;  // whole stage sets per issuer
+    if (stages < std::max(C::kIssuers, 4) || ring_bytes(stages) > budget) return false;
+    size_t smem = 1024 + ring_bytes(stages) + part_bytes + bar_bytes;
+    smem = std::max<size_t>(smem, kMinSmemPerCta);
+    if (smem > kMaxDynSmem) return false;
+    stages_out = stages;
+    smem_o = smem;
+    return true;
+  };
+  int stages1 = 0, stagesN = 0;
+  size_t smem1 = 0, smemN = 0;
+  const bool ok1 = layout(false, stages1, smem1), okN = layout(true, stagesN, smemN);
+  if (!ok1 && !okN) return false;
 
   // Model (measured on GB300 with TMA streams of 128-byte rows): one SM
   // streams ~45 GB/s; all SMs together ~4.8 TB/s with 128-row boxes and
@@ -648,6 +663,8 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
   const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (split > args.num_kb || (BN / 8) / split < 1) break;
+    if (!(split == 1 ? ok1 : okN)) continue;
+    const size_t smem = split == 1 ? smem1 : smemN;
     const int active = max_active_clusters<BN, kQ>(split, smem);
     if (active <= 0) continue;
     int clusters = std::min(active, args.num_nb);
@@ -662,9 +679,14 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
       plan.cost = cost;
       plan.split = split;
       plan.clusters = clusters;
+      plan.stages = split == 1 ? stages1 : stagesN;
+      plan.smem = smem;
     }
   }
-  return plan.split > 0;
+  if (plan.split <= 0) return false;
+  args.num_stages = plan.stages;
+  smem_out = plan.smem;
+  return true;
 }
 
 // Allows the kernel its shared memory on the current device (once per device);
