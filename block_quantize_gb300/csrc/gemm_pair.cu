@@ -16,9 +16,9 @@
 // many FP32 accumulators in registers, and each SM stages only its half of B.
 //
 //   * CTA r of a pair loads A rows [256 pm + 128 r, +128) (warp 0) and B rows
-//     [128 nb + 64 r, +64) (the last warp) of every K block with TMA; all loads
-//     count on the even CTA's `full` barrier, which the even CTA arms for both
-//     CTAs' bytes;
+//     [128 nb + 64 r, +64) (the last warp; warp 0 too in the requantizing
+//     instantiation) of every K block with TMA; all loads count on the even
+//     CTA's `full` barrier, which the even CTA arms for both CTAs' bytes;
 //   * warps 1 and 2 of the even CTA take turns issuing the four MMAs (K = 32)
 //     of a K block into TMEM buffer it % 4 of both CTAs; each commit arrives on
 //     the stage's `empty` barrier and the buffer's `tfull` barrier in both
@@ -71,8 +71,10 @@ struct PCfg {
   static constexpr int kEpiPerQuad = kBN / kEpiCols;  // warps per TMEM lane quadrant
   static constexpr int kEpiWarps = 4 * kEpiPerQuad;
   static constexpr int kFirstEpiWarp = 1 + kIssuers;
-  static constexpr int kBProducer = kFirstEpiWarp + kEpiWarps;  // the last warp loads B
-  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps + 1);
+  // bf16 output: the last warp loads B. The requantizing epilogue keeps one
+  // producer for both operands (measured 3-7 % faster there).
+  static constexpr int kBProducer = kFirstEpiWarp + kEpiWarps;
+  static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps + (kQ ? 0 : 1));
   // bf16 output: staging boxes for the TMA stores; E4M3 output: the slices'
   // maxima exchange (codes are stored straight from registers).
   static constexpr uint32_t kOutBytes =
@@ -247,10 +249,10 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0)
-      loads_issued = pair_producer<kNT, kKG, 1>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair,
-                                                num_pairs, abort_flag, status);
+      loads_issued = pair_producer<kNT, kKG, kQ ? 0 : 1>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar,
+                                                         rank, pair, num_pairs, abort_flag, status);
     __syncwarp();
-  } else if (warp == C::kBProducer) {
+  } else if (!kQ && warp == C::kBProducer) {
     // ---------------------------------------------------------- B producer --
     if (lane == 0)
       pair_producer<kNT, kKG, 2>(tmap_a, tmap_b, args, smem_u32(ring), full_bar, empty_bar, rank, pair, num_pairs,
