@@ -131,6 +131,44 @@ __device__ __forceinline__ uint32_t encode4_pairs(uint64_t v01, uint64_t v23, fl
   return cvt2(va.x / s, va.y / s) | (cvt2(vb.x / s, vb.y / s) << 16);
 }
 
+// encode4_pairs over a 64-column row slice (16 groups of four): every group's
+// codes are formed before any fallback division, so the groups' independent
+// multiplies and conversions can interleave (a division branch per group
+// serialized them). The codes are those of encode4_pairs.
+__device__ __forceinline__ void encode64_pairs(const uint64_t (&acc)[32], uint32_t (&code)[16], float s, uint64_t r2,
+                                               bool pow2) {
+  if (pow2) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float2 a = f32x2_split(fmul2(acc[2 * j], r2)), b = f32x2_split(fmul2(acc[2 * j + 1], r2));
+      code[j] = cvt2(a.x, a.y) | (cvt2(b.x, b.y) << 16);  // q = v / s exactly
+    }
+    return;
+  }
+  const uint64_t lo2 = f32x2(__float_as_uint(1.0f - 0x1p-20f), __float_as_uint(1.0f - 0x1p-20f));
+  const uint64_t hi2 = f32x2(__float_as_uint(1.0f + 0x1p-20f), __float_as_uint(1.0f + 0x1p-20f));
+  uint32_t bad = s >= 0x1p-126f ? 0u : 0xFFFFu;  // a subnormal scale is always divided
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint64_t q01 = fmul2(acc[2 * j], r2), q23 = fmul2(acc[2 * j + 1], r2);
+    const float2 la = f32x2_split(fmul2(q01, lo2)), lb = f32x2_split(fmul2(q23, lo2));
+    const float2 ha = f32x2_split(fmul2(q01, hi2)), hb = f32x2_split(fmul2(q23, hi2));
+    const uint32_t lo = cvt2(la.x, la.y) | (cvt2(lb.x, lb.y) << 16);
+    const uint32_t hi = cvt2(ha.x, ha.y) | (cvt2(hb.x, hb.y) << 16);
+    code[j] = lo;
+    bad |= (lo == hi ? 0u : 1u) << j;
+  }
+  if (bad != 0u) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if ((bad >> j) & 1u) {
+        const float2 va = f32x2_split(acc[2 * j]), vb = f32x2_split(acc[2 * j + 1]);
+        code[j] = cvt2(va.x / s, va.y / s) | (cvt2(vb.x / s, vb.y / s) << 16);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Requantizing GEMM epilogue.
 //
@@ -237,8 +275,11 @@ __device__ __forceinline__ bool requant_store_slice(const uint64_t (&acc)[32], b
 
   const uint64_t r2 = f32x2(__float_as_uint(r), __float_as_uint(r));
   uint32_t code[16];
+  encode64_pairs(acc, code, s, r2, pow2);
+  if (!row_valid) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) code[j] = row_valid ? encode4_pairs(acc[2 * j], acc[2 * j + 1], s, r2, pow2) : 0u;
+    for (int j = 0; j < 16; ++j) code[j] = 0u;
+  }
 
   if (col0 + 64 <= N && tmap_q != nullptr) {
     if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last store has read the box
