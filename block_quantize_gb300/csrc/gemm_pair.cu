@@ -30,8 +30,11 @@
 //     rounded like fmaf). After the last K block each warp rounds its 32 x 32
 //     boxes to bf16 and writes them with TMA stores clipped at the M and N edges;
 //   * pairs are persistent over the 256x128 tiles in a grouped raster.
-// M-grouped calls (MoE experts, pzsr.cn page §2.3, §3.2) run on the same
-// kernels: both 128-row halves of a pair tile multiply one B, so a pair row
+// K-grouped calls (one output per range of K, pzsr.cn page §3.2) run this
+// kernel over every range's tiles in one launch (see KUnit).
+// M-grouped calls (MoE experts, pzsr.cn page §2.3, §3.2) with power-of-two
+// scales run on the block-scaled kernel below (with FP32 scales, on the 1-SM
+// kernel of gemm.cu): both 128-row halves of a pair tile multiply one B, so a pair row
 // whose two blocks belong to one expert is one unit, and a pair row whose
 // blocks belong to different experts (or to an expert and padding) becomes
 // two units, each with one CTA keeping its rows and the other discarding its
