@@ -23,7 +23,7 @@ def _gpu_quant(x, mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-@pytest.mark.parametrize("shape", [(1, 128), (7, 300), (130, 1000), (257, 2048), (3, 5)])
+@pytest.mark.parametrize("shape", [(1, 128), (7, 300), (130, 1000), (257, 2048), (3, 5), (80000, 100), (30000, 300)])
 def test_quantize_fp32_bit_exact(oracle_mod, mode, shape):
     x = synthetic.lognormal_rows(shape, seed=shape[0] * 13 + shape[1])
     x[0, : min(3, shape[1])] = 0.0
@@ -37,7 +37,7 @@ def test_quantize_fp32_bit_exact(oracle_mod, mode, shape):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-@pytest.mark.parametrize("shape", [(5, 128), (64, 777), (300, 4096)])
+@pytest.mark.parametrize("shape", [(5, 128), (64, 777), (300, 4096), (80000, 100), (30000, 300)])
 def test_quantize_bf16_bit_exact(oracle_mod, mode, shape):
     """bfloat16 input: the oracle gets the exact FP32 values of the same bf16s."""
     x = torch.from_numpy(synthetic.lognormal_rows(shape, seed=shape[1] + 5)).to(torch.bfloat16)

@@ -29,7 +29,11 @@ def _check(x_np, mode, oracle_mod, x_dev=None):
 
 @pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("shape", [(128, 128), (1, 1), (1, 7), (3, 130), (129, 130), (300, 513),
-                                   (255, 1024), (128, 512), (1000, 4)])
+                                   (255, 1024), (128, 512), (1000, 4),
+                                   # more blocks than four per SM (the 3-stage streaming launch):
+                                   # one block per row of blocks, and rows of three blocks that
+                                   # the grid's stride wraps unevenly
+                                   (80000, 100), (30000, 300)])
 def test_quantize_bit_exact(oracle_mod, shape, mode):
     _check(synthetic.lognormal_rows(shape, seed=101 + shape[0] + shape[1]), mode, oracle_mod)
 
