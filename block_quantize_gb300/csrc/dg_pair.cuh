@@ -231,6 +231,53 @@ __device__ __forceinline__ void store_tile_rows(const uint64_t (&acc)[EC / 2], c
   }
 }
 
+// bf16 epilogue of one warp with one 32 x 64 box: 128-byte rows in the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)), one TMA
+// store per warp and tile. A slice that crosses column N is written element
+// by element.
+template <bool k3D = false>
+__device__ __forceinline__ void store_tile_rows64(const uint64_t (&acc)[32], const CUtensorMap& tmap_c,
+                                                  const PairArgs& args, uint8_t* box, int row0, int col0, int lane,
+                                                  bool& stores_issued, int g = 0) {
+  if (lane == 0 && stores_issued) bulk_wait_read_all();  // the last tile's store has read the box
+  __syncwarp();
+  if (col0 + 64 > args.N) {
+    const int row = row0 + lane;
+    if (row < args.M && col0 < args.N) {
+      __nv_bfloat16* crow = args.c + (static_cast<int64_t>(g) * args.M + row) * args.ld_c;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float2 v = f32x2_split(acc[j]);
+        if (col0 + 2 * j < args.N) crow[col0 + 2 * j] = __float2bfloat16_rn(v.x);
+        if (col0 + 2 * j + 1 < args.N) crow[col0 + 2 * j + 1] = __float2bfloat16_rn(v.y);
+      }
+    }
+    return;
+  }
+  uint8_t* my_row = box + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float2 v0 = f32x2_split(acc[c * 4]), v1 = f32x2_split(acc[c * 4 + 1]);
+    const float2 v2 = f32x2_split(acc[c * 4 + 2]), v3 = f32x2_split(acc[c * 4 + 3]);
+    uint4 pk;
+    pk.x = pack_bf16(v0.x, v0.y);
+    pk.y = pack_bf16(v1.x, v1.y);
+    pk.z = pack_bf16(v2.x, v2.y);
+    pk.w = pack_bf16(v3.x, v3.y);
+    *reinterpret_cast<uint4*>(my_row + ((c ^ (lane & 7)) << 4)) = pk;
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < args.M) {
+    if constexpr (k3D)
+      tma_store_3d(&tmap_c, smem_u32(box), col0, row0, g);
+    else
+      tma_store_2d(&tmap_c, smem_u32(box), col0, row0);
+    bulk_commit();
+    stores_issued = true;
+  }
+}
+
 // The same store for a row slice already rounded to bf16: pk[j] holds columns
 // col0 + 2 j and col0 + 2 j + 1; one staging box per warp, reused for the
 // second 32-column half once its first store has read it.

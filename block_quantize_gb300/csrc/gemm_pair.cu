@@ -27,8 +27,9 @@
 //   * the epilogue warps of each CTA read their 32 TMEM lanes of the partial,
 //     release the buffer by arriving on the even CTA's `tempty` barrier, and
 //     promote it in registers (two FP32 FMAs per f32x2 instruction, each
-//     rounded like fmaf). After the last K block each warp rounds its 32 x 32
-//     boxes to bf16 and writes them with TMA stores clipped at the M and N edges;
+//     rounded like fmaf). After the last K block each warp rounds its 32 x 64
+//     slice to bf16 and writes it with one TMA store (128-byte swizzle) clipped
+//     at M; a slice that crosses N is written element by element;
 //   * pairs are persistent over the 256x128 tiles in a grouped raster.
 // K-grouped calls (one output per range of K, pzsr.cn page §3.2) run this
 // kernel over every range's tiles in one launch (see KUnit).
@@ -392,8 +393,7 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
           break;
         }
       } else {
-        store_tile_rows<EC, EC / 32, kKG>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane,
-                                          stores_issued, u.g);
+        store_tile_rows64<kKG>(acc, tmap_c, args, out_box, row0, nb * kBN + part * EC, lane, stores_issued, u.g);
       }
     }
     if (lane == 0 && stores_issued) bulk_wait_all();
@@ -1172,12 +1172,13 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
                                    CU_TENSOR_MAP_SWIZZLE_64B))
       return DG_ERR_CUDA;
   } else {
-    // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle.
+    // C as bf16 [M][ld_c]: 32 x 32 boxes, 64-byte swizzle (the FP32-promotion
+    // kernel: 32 x 64 boxes, 128-byte swizzle).
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(p.ld_c) * 2};
-    const uint32_t box[2] = {32, 32};
+    const uint32_t box[2] = {scaled ? 32u : 64u, 32};
     if (!encode_tensor_map_swizzle(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.c, 2, dims, strides, box,
-                                   CU_TENSOR_MAP_SWIZZLE_64B))
+                                   scaled ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return DG_ERR_CUDA;
   }
 
@@ -1282,9 +1283,9 @@ int launch_gemm_pair_k_grouped(const GemmProblem& p, const int64_t* k_sizes, int
     const uint64_t dims[3] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M),
                               static_cast<uint64_t>(num_groups)};
     const uint64_t str[2] = {static_cast<uint64_t>(p.ld_c) * 2, static_cast<uint64_t>(p.ld_c) * 2 * p.M};
-    const uint32_t box[3] = {32, 32, 1};
+    const uint32_t box[3] = {64, 32, 1};
     if (!encode_tensor_map_swizzle(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.c, 3, dims, str, box,
-                                   CU_TENSOR_MAP_SWIZZLE_64B))
+                                   CU_TENSOR_MAP_SWIZZLE_128B))
       return DG_ERR_CUDA;
   }
   const cudaError_t e = launch_kernel(fp8_gemm_pair_kernel<kEpiCols, false, false, true>, dim3(2 * pairs),
