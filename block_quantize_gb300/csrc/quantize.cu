@@ -29,8 +29,9 @@
 //    floats): one persistent CTA per SM streams 128x128 FP32 blocks (64 KB)
 //    through a 3-stage TMA ring in shared memory guarded by mbarriers, two
 //    blocks ahead of the one being reduced and encoded (inputs of at most four
-//    blocks per SM: two single-stage CTAs per SM instead). Each block is copied
-//    from shared memory to registers once. Out-of-range rows and columns of
+//    or three blocks per SM: two or three single-stage CTAs per SM instead).
+//    Each block is copied from shared memory to registers once (three CTAs
+//    per SM: twice, for the block max and for the encode). Out-of-range rows and columns of
 //    edge blocks arrive as zeros (TMA fill), which leaves the block max
 //    unchanged.
 //  * quantize_kernel (any alignment): one CTA per block, the block held in
@@ -90,6 +91,45 @@ __device__ __forceinline__ void encode_store(const float4 (&v)[kRowsPerWarp], in
 #pragma unroll
       for (int t = 0; t < 4; ++t)
         if (c0 + t < cols) out[t] = encode1<kMode>(e[t], s, r);
+    }
+  }
+}
+
+// encode_store for a tile that stays in shared memory (kThreads threads, FP32
+// 128 x 128, row-major): this thread's eight rows are read again and encoded
+// four at a time, which holds 16 input registers instead of 32.
+template <bool kPow2>
+__device__ __forceinline__ void encode_store_reread(const uint8_t* tile, int warp, int lane, int64_t r0, int64_t c0,
+                                                    int64_t rows, int64_t cols, uint8_t* __restrict__ q,
+                                                    int64_t ld_q, float s, float r) {
+  const bool inside = r0 + kRowsPerWarp <= rows && c0 + 3 < cols;
+#pragma unroll
+  for (int h = 0; h < kRowsPerWarp / 4; ++h) {
+    float4 w[4];
+    uint32_t code[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = reinterpret_cast<const float4*>(tile + (warp * kRowsPerWarp + h * 4 + i) * kBlock * 4)[lane];
+    if constexpr (kPow2)
+      encode4_n<1>(w, code, s, r);
+    else if (s >= 0x1p-126f)
+      encode4_n<0>(w, code, s, r);
+    else
+      encode4_n<2>(w, code, s, r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t row = r0 + h * 4 + i;
+      uint8_t* out = q + row * ld_q + c0;
+      if (inside) {
+        __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
+      } else if (row < rows) {
+        if (c0 + 3 < cols) {
+          __stcs(reinterpret_cast<unsigned int*>(out), code[i]);
+        } else {
+          for (int t = 0; t < 4; ++t)
+            if (c0 + t < cols) out[t] = static_cast<uint8_t>((code[i] >> (8 * t)) & 0xFFu);
+        }
+      }
     }
   }
 }
@@ -262,26 +302,35 @@ __global__ void __launch_bounds__(k1xThreads) quantize_1x128_kernel(
 // freed an iteration earlier, which keeps two 64 KB FP32 blocks per SM in
 // flight (measured on GB300: 16384x7168 FP32 quantized at 6.9 TB/s against
 // 6.45 TB/s with three in flight).
-// kShort: one stage and two CTAs per SM (64 registers per thread), for inputs
-// of at most four blocks per SM. Each SM then encodes two blocks at once
-// instead of one after the other once the last loads land (measured: 4096x2048
-// FP32 in 8.2 us against 8.6 us).
+// kShort = 2: one stage and two CTAs per SM (64 registers per thread), for
+// inputs of at most four blocks per SM. Each SM then encodes two blocks at
+// once instead of one after the other once the last loads land (measured:
+// 4096x2048 FP32 in 8.2 us against 8.6 us).
+// kShort = 3: one stage and three CTAs per SM, for inputs of at most three
+// blocks per SM, so that every block is resident from the start and no SM
+// takes a second round. Three 64 KB tiles leave 42 registers per thread, too
+// few to hold a tile between the block max and the encode, so the encode
+// reads the tile from shared memory a second time, four rows at a time
+// (measured: 4096x1536 FP32 in 6.68 us against 6.99 us; at 512 blocks the
+// two-CTA form stays 1-2 % faster).
 // bfloat16 tiles (32 KB) carry half the bytes of FP32 ones for the same
 // arithmetic, so that kernel is bound by instruction latency with one CTA's
 // 16 warps per SM: it runs two CTAs of three stages per SM (measured:
 // 16384x7168 row-wise in 73.5 us against 92.5 us with one CTA of six stages).
-template <bool kBf16, bool kShort = false>
+template <bool kBf16, int kShort = 0>
 struct StreamCfg {
+  static_assert(kShort == 0 || ((kShort == 2 || kShort == 3) && !kBf16), "short-input forms: FP32 tiles");
   static constexpr int kElemBytes = kBf16 ? 2 : 4;
   static constexpr uint32_t kTileBytes = kBlock * kBlock * kElemBytes;
-  static constexpr int kStages = kBf16 ? 3 : (kShort ? 1 : 3);
+  static constexpr int kStages = kShort ? 1 : 3;
   static constexpr int kAhead = kStages > 1 ? kStages - 1 : 1;
-  static constexpr int kCtasPerSm = (kShort || kBf16) ? 2 : 1;
+  static constexpr int kCtasPerSm = kShort ? kShort : (kBf16 ? 2 : 1);
+  static constexpr bool kReread = kShort == 3;  // encode from shared memory, not registers
 };
 
 // kRowwise: one scale per row of the tile (1 x 128 blocks) instead of one per
 // tile; kBf16: bfloat16 input tiles, widened to FP32 exactly.
-template <bool kPow2, bool kRowwise, bool kBf16, bool kShort>
+template <bool kPow2, bool kRowwise, bool kBf16, int kShort>
 __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm)
     quantize_stream_kernel(const __grid_constant__ CUtensorMap tmap_x, int64_t rows, int64_t cols,
                            uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ scales,
@@ -429,8 +478,9 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
       const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
       if (lane == 0) warp_amax[warp] = __uint_as_float(wmax);
       __syncthreads();  // also: every thread has copied its part of the stage
-      // Every thread has copied block j: the stage of block j + kAhead is free.
-      if (threadIdx.x == 0) issue(j + kAhead);
+      // Every thread has copied block j: the stage of block j + kAhead is free
+      // (re-reading forms: once the encode below has read it again).
+      if (!SC::kReread && threadIdx.x == 0) issue(j + kAhead);
       float amax = warp_amax[0];
 #pragma unroll
       for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, warp_amax[w]);
@@ -439,14 +489,17 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
       if constexpr (kPow2) s = pow2_round_up(s);
       if (threadIdx.x == 0) scales[blk] = s;
       const float r = 1.0f / s;
-      if constexpr (kPow2) {
+      if constexpr (SC::kReread) {
+        encode_store_reread<kPow2>(stage_data + st * SC::kTileBytes, warp, lane, r0, c0, rows, cols, q, ld_q, s, r);
+      } else if constexpr (kPow2) {
         encode_store<1, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
       } else if (s >= 0x1p-126f) {
         encode_store<0, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
       } else {
         encode_store<2, true>(v, r0, c0, rows, cols, q, ld_q, s, r);
       }
-      __syncthreads();  // warp_amax is rewritten by the next block
+      __syncthreads();  // warp_amax is rewritten by the next block; the stage is read
+      if (SC::kReread && threadIdx.x == 0) issue(j + kAhead);
     }
     if (++st == kStages) {
       st = 0;
@@ -475,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, StreamCfg<kBf16, kShort>::kCtasPerSm
 
 // Launch the streaming kernel (16-byte-aligned x, row stride a multiple of 16
 // bytes); false if the tensor map cannot be made (the caller falls back).
-template <bool kPow2, bool kRowwise, bool kBf16, bool kShort = false>
+template <bool kPow2, bool kRowwise, bool kBf16, int kShort = 0>
 bool launch_stream(const void* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q, int64_t ld_q,
                    float* scales, cudaStream_t stream, cudaError_t& err) {
   using SC = StreamCfg<kBf16, kShort>;
@@ -586,12 +639,17 @@ cudaError_t launch_quantize(const float* x, int64_t rows, int64_t cols, int64_t 
   if (vec) {
     int dev = 0;
     const int sms = cudaGetDevice(&dev) == cudaSuccess ? device_sm_count(dev) : 0;
-    const bool short_input = sms > 0 && nblocks <= 4 * static_cast<int64_t>(sms);
+    // Short inputs: every block resident at once with three CTAs per SM, else
+    // two per SM while the input has at most four blocks per SM.
+    const int64_t per_sm = sms > 0 ? (nblocks + sms - 1) / sms : 0;
     cudaError_t err = cudaSuccess;
     bool done;
-    if (short_input)
-      done = pow2_scales ? launch_stream<true, false, false, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
-                         : launch_stream<false, false, false, true>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    if (sms > 0 && per_sm <= 3)
+      done = pow2_scales ? launch_stream<true, false, false, 3>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, false, false, 3>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
+    else if (sms > 0 && per_sm <= 4)
+      done = pow2_scales ? launch_stream<true, false, false, 2>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
+                         : launch_stream<false, false, false, 2>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);
     else
       done = pow2_scales ? launch_stream<true, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err)
                          : launch_stream<false, false, false>(x, rows, cols, ld_x, q, ld_q, scales, stream, err);

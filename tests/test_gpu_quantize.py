@@ -33,7 +33,12 @@ def _check(x_np, mode, oracle_mod, x_dev=None):
                                    # more blocks than four per SM (the 3-stage streaming launch):
                                    # one block per row of blocks, and rows of three blocks that
                                    # the grid's stride wraps unevenly
-                                   (80000, 100), (30000, 300)])
+                                   (80000, 100), (30000, 300),
+                                   # on 152 SMs: at most three blocks per SM (three CTAs per SM,
+                                   # the tile re-read from shared memory), whole and ragged ...
+                                   (4096, 1536), (3000, 1500),
+                                   # ... and four blocks per SM (two CTAs per SM)
+                                   (4096, 2048), (4000, 2000)])
 def test_quantize_bit_exact(oracle_mod, shape, mode):
     _check(synthetic.lognormal_rows(shape, seed=101 + shape[0] + shape[1]), mode, oracle_mod)
 
