@@ -8,8 +8,9 @@
 //
 // One CTA of 512 threads owns one 128x128 block: warp w holds rows
 // [8w, 8w+8), lane l holds columns [4l, 4l+4), i.e. 8 float4 per thread kept in
-// registers between the two passes, so the input is read from HBM once; small
-// CTAs let four blocks stay resident per SM, keeping enough loads in flight.
+// registers between the two passes, so the input is read from HBM once.
+// quantize_kernel (below) runs one such CTA per block; at 64-87 registers a
+// thread one or two of them are resident per SM.
 // Loads are 128-bit and streaming; each warp-wide load covers one 512-byte row
 // segment. The block max is a warp-shuffle reduction followed by a 16-entry
 // shared-memory reduction (warp-shuffle reduction as in the hotelren.com GEMM
