@@ -800,18 +800,21 @@ def run_aux(args):
     elif kind == "kgrouped":
         # K-grouped TN GEMM shaped like an MoE weight gradient: dW_g [N_int, hidden]
         # = dY_g^T X_g over the tokens routed to expert g (padded to 128).
+        # kgrouped:ue8m0 takes power-of-two scales.
+        mode = 1 if spec == "ue8m0" else 0
         mo = synthetic.MOE
         sizes = synthetic.moe_group_sizes(mo["experts"], mo["tokens"], mo["topk"], 0)
         sizes = [int(-(-int(v) // 128) * 128) for v in sizes]
         m, n, k_tot = mo["intermediate"], mo["hidden"], sum(sizes)
-        qa, sa = _rand_fp8((m, k_tot), dev, gen, 0)
-        qb, sb = _rand_fp8((n, k_tot), dev, gen, 0)
+        qa, sa = _rand_fp8((m, k_tot), dev, gen, mode)
+        qb, sb = _rand_fp8((n, k_tot), dev, gen, mode)
         a_st, b_st = qa.t().contiguous(), qb.t().contiguous()
         c = torch.empty((len(sizes), m, n), dtype=torch.bfloat16, device=dev)
-        ms = _time_each(stream, [lambda: bq.dg_fp8_k_grouped_gemm_tn(c, a_st, b_st, sa, sb, sizes)],
+        ms = _time_each(stream, [lambda: bq.dg_fp8_k_grouped_gemm_tn(c, a_st, b_st, sa, sb, sizes, mode)],
                         args.steps, args.warmup)[0]
         fl = 2.0 * m * n * k_tot
-        out["results"] = [{"M": m, "N": n, "K_tot": k_tot, "groups": sizes, "us": ms * 1e3,
+        out["results"] = [{"M": m, "N": n, "K_tot": k_tot, "groups": sizes, "scales": "ue8m0" if mode else "fp32",
+                           "us": ms * 1e3,
                            "tflops": fl / (ms * 1e-3) / 1e12,
                            "frac_fp8_burst": fl / (ms * 1e-3) / 1e12 / fp8_peak}]
     elif kind == "grouped":
@@ -837,7 +840,7 @@ def main():
     p.add_argument("--workload", default="llm",
                    help="llm (the benchmark line) | gemm:M,N,K[:ue8m0] | square[:ue8m0] | small | "
                         "quantize[:R,C] | grouped | quantize1x128[:R,C] | gemm1x128[:M,N,K] | "
-                        "requant[:M,N,K[:variant]] | layouts[:M,N,K] | kgrouped | cpu_baseline  "
+                        "requant[:M,N,K[:variant]] | layouts[:M,N,K] | kgrouped[:ue8m0] | cpu_baseline  "
                         "(the others print per-kernel numbers for profiling)")
     args = p.parse_args()
     if args.steps is None:

@@ -32,7 +32,8 @@
 //     at M; a slice that crosses N is written element by element;
 //   * pairs are persistent over the 256x128 tiles in a grouped raster.
 // K-grouped calls (one output per range of K, pzsr.cn page §3.2) run this
-// kernel over every range's tiles in one launch (see KUnit).
+// kernel (FP32 scales; see KUnit) or the block-scaled kernel below
+// (power-of-two scales; see ScaledUnit) over every range's tiles in one launch.
 // M-grouped calls (MoE experts, pzsr.cn page §2.3, §3.2) with power-of-two
 // scales run on the block-scaled kernel below (with FP32 scales, on the 1-SM
 // kernel of gemm.cu): both 128-row halves of a pair tile multiply one B, so a pair row
@@ -512,13 +513,49 @@ __device__ __forceinline__ uint32_t ue8m0_word(float s) {
   return 0x01010101u * ((__float_as_uint(s) >> 23) & 0xFFu);
 }
 
-template <bool kQ, bool kNT, bool kGrouped, int kBNs>
+// A unit of the block-scaled kernel: the pair unit, its K blocks
+// [kb0, kb0 + nkb) and its output matrix. K-grouped calls: unit t is tile
+// t % T of range t / T (T = num_pm * num_nb tiles per range); otherwise all
+// of K and matrix 0.
+struct ScaledUnit {
+  PairUnit u;
+  int kb0, nkb, gout;
+};
+template <bool kKG, class Args>
+__device__ __forceinline__ int scaled_num_units(const Args& a) {
+  if constexpr (kKG)
+    return a.num_kg * a.num_pm * a.num_nb;
+  else
+    return pair_num_units(a);
+}
+template <bool kGrouped, bool kKG, class Args>
+__device__ __forceinline__ ScaledUnit scaled_unit(int t, const Args& a, const UnitIds& ids) {
+  ScaledUnit s;
+  if constexpr (kKG) {
+    const int per = a.num_pm * a.num_nb;
+    const int i = t / per;
+    s.u = pair_unit<false>(t - i * per, a, ids);
+    s.kb0 = a.kb_lo[i];
+    s.nkb = a.kb_n[i];
+    s.gout = a.g_out[i];
+  } else {
+    s.u = pair_unit<kGrouped>(t, a, ids);
+    s.kb0 = 0;
+    s.nkb = a.num_kb;
+    s.gout = 0;
+  }
+  return s;
+}
+
+template <bool kQ, bool kNT, bool kGrouped, int kBNs, bool kKG = false>
 __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
     fp8_gemm_pair_scaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
-                                const __grid_constant__ CUtensorMap tmap_c, const PairArgsT<kQ, kGrouped> args) {
+                                const __grid_constant__ CUtensorMap tmap_c,
+                                const std::conditional_t<kKG, PairArgsKG, PairArgsT<kQ, kGrouped>> args) {
   using NC = NatCfg<kBNs>;
   static_assert(kBNs == 128 || (!kQ && kNT), "256-column pair tiles: bf16 output, NT layout");
+  static_assert(!kKG || (!kQ && !kGrouped && kBNs == 128), "K-grouped calls: bf16 output, 128-column tiles");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -551,7 +588,9 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < NC::kNumAcc; ++b) {
-      mbar_init(smem_u32(&tfull_bar[b]), nst >= 2 ? 2 : 1);  // one commit per issuer with stages in the tile
+      // One commit per issuer with stages in the tile (K-grouped units of one
+      // stage: its issuer commits twice).
+      mbar_init(smem_u32(&tfull_bar[b]), (kKG || nst >= 2) ? 2 : 1);
       mbar_init(smem_u32(&tempty_bar[b]), 2 * NC::kEpiWarps);
     }
     mbar_init(smem_u32(drain_bar), 2);
@@ -571,7 +610,7 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  const int num_units = pair_num_units(args);
+  const int num_units = scaled_num_units<kKG>(args);
   uint32_t loads_issued = 0;
 
   if (warp == 0 || warp == 3) {
@@ -588,13 +627,15 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
       for (int t = pair; t < num_units && ok; t += num_pairs) {
         const UnitIds cur = nxt;
         nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
-        const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+        const ScaledUnit su = scaled_unit<kGrouped, kKG>(t, args, cur);
+        const PairUnit& u = su.u;
+        const int unst = kKG ? (su.nkb + NC::kKbPerStage - 1) / NC::kKbPerStage : nst;  // stages of the unit
         for (int slot = 0; slot < u.nslots && ok; ++slot) {
         const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
         if (!ps.mma) continue;
         const int arow = u.pm * (2 * kBM) + static_cast<int>(rank) * kBM;
         const int brow = u.nb * kBNs + static_cast<int>(rank) * (kBNs / 2);
-        for (int sl = 0; sl < nst; ++sl, ++g) {
+        for (int sl = 0; sl < unst; ++sl, ++g) {
           if ((g & 1u) != me) continue;
           if (!kGrouped || lane == 0) {
             ok = mbar_wait(empty0 + stage * 8u, phase ^ 1u, abort_flag, status, limit);
@@ -605,16 +646,17 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
               // K-major: 3-D maps {128, rows, K/128} (M-grouped B: 4-D with the
               // expert last); MN-major: 2-D maps {rows, K} whose 256-row boxes
               // stack the stage's two K blocks.
+              const int kbs = su.kb0 + sl * NC::kKbPerStage;  // first K block of the stage
               if (!kNT && args.a_mn)
-                tma_load_2d_pair(dst, &tmap_a, fb, arow, sl * NC::kKbPerStage * kBK);
+                tma_load_2d_pair(dst, &tmap_a, fb, arow, kbs * kBK);
               else
-                tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, sl * NC::kKbPerStage);
+                tma_load_3d_pair(dst, &tmap_a, fb, 0, arow, kbs);
               if constexpr (kGrouped)
-                tma_load_4d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, sl * NC::kKbPerStage, ps.g);
+                tma_load_4d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, kbs, ps.g);
               else if (!kNT && args.b_mn)
-                tma_load_2d_pair(dst + NC::kAStage, &tmap_b, fb, brow, sl * NC::kKbPerStage * kBK);
+                tma_load_2d_pair(dst + NC::kAStage, &tmap_b, fb, brow, kbs * kBK);
               else
-                tma_load_3d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, sl * NC::kKbPerStage);
+                tma_load_3d_pair(dst + NC::kAStage, &tmap_b, fb, 0, brow, kbs);
               ++loads_issued;
             }
           }
@@ -648,12 +690,14 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
       for (int t = pair; t < num_units && ok; t += num_pairs) {
         const UnitIds cur = nxt;
         nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
-        const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+        const ScaledUnit su = scaled_unit<kGrouped, kKG>(t, args, cur);
+        const PairUnit& u = su.u;
+        const int unst = kKG ? (su.nkb + NC::kKbPerStage - 1) / NC::kKbPerStage : nst;  // stages of the unit
         for (int slot = 0; slot < u.nslots && ok; ++slot) {
         if (!pair_slot<kGrouped>(u, slot, args).mma) continue;
         const uint32_t abuf = tl % NC::kNumAcc;
         const uint32_t d = tmem_base + abuf * kBNs;
-        for (int sl = 0; sl < nst; ++sl, ++g) {
+        for (int sl = 0; sl < unst; ++sl, ++g) {
           if ((g & 1u) != me) continue;
           if (!kGrouped || lane == 0) {
             ok = mbar_wait(full0 + stage * 8u, sphase, abort_flag, status, limit);
@@ -683,7 +727,7 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < NC::kKbPerStage; ++j) {
               const int kb = sl * NC::kKbPerStage + j;
-              if (kb < args.num_kb) {
+              if (kb < su.nkb) {
                 const uint32_t sfa = tmem_base + NC::kAccCols + (stage * NC::kKbPerStage + j) * NC::kSfCols;
                 if constexpr (kNT) {
                   const uint64_t adesc = sw128_kmajor_desc(base + j * kABytes);
@@ -703,7 +747,10 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
               }
             }
             mma_commit_pair_mc(empty0 + stage * 8u, 0x3);
-            if (sl + 2 >= nst) mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
+            if (sl + 2 >= unst) {
+              mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
+              if (kKG && unst == 1) mma_commit_pair_mc(smem_u32(&tfull_bar[abuf]), 0x3);
+            }
             *issue_turn = g + 1;
           }
           stage += 2;
@@ -728,7 +775,9 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
     for (int t = pair; t < num_units && ok; t += num_pairs) {
       const UnitIds cur = nxt;
       nxt = pair_unit_ids<kGrouped>(t + num_pairs, args, lane);
-      const PairUnit u = pair_unit<kGrouped>(t, args, cur);
+      const ScaledUnit su = scaled_unit<kGrouped, kKG>(t, args, cur);
+      const PairUnit& u = su.u;
+      const int unst = kKG ? (su.nkb + NC::kKbPerStage - 1) / NC::kKbPerStage : nst;  // stages of the unit
       for (int slot = 0; slot < u.nslots && ok; ++slot) {
       const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
       if (!ps.mma) continue;
@@ -740,9 +789,9 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
       const int nbs = (args.N + kBK - 1) / kBK;  // 128-row scale blocks of B (per expert)
       const float* sb_p = args.sb + (static_cast<int64_t>(ps.g) * nbs + sbb) * args.ld_sb;
       const float* sb_hi = sb_p + (sbb + 1 < nbs ? args.ld_sb : 0);
-      for (int sl = 0; sl < nst; ++sl) {
-        const int kb0 = sl * NC::kKbPerStage;
-        const bool two = NC::kKbPerStage == 2 && kb0 + 1 < args.num_kb;
+      for (int sl = 0; sl < unst; ++sl) {
+        const int kb0 = su.kb0 + sl * NC::kKbPerStage;
+        const bool two = NC::kKbPerStage == 2 && sl * NC::kKbPerStage + 1 < su.nkb;
         const uint32_t ea0 = ue8m0_word(__ldg(sa_p + kb0)), eb0 = ue8m0_word(__ldg(sb_p + kb0));
         const uint32_t ea1 = two ? ue8m0_word(__ldg(sa_p + kb0 + 1)) : ea0;
         const uint32_t eb1 = two ? ue8m0_word(__ldg(sb_p + kb0 + 1)) : eb0;
@@ -786,7 +835,8 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
     for (int t = pair; t < num_units && ok; t += num_pairs) {
       // No look-ahead here: the epilogue waits a whole tile for its accumulator,
       // and the prefetched ids would cost registers that its loads need.
-      const PairUnit u = pair_unit<kGrouped>(t, args, pair_unit_ids<kGrouped>(t, args, lane));
+      const ScaledUnit su = scaled_unit<kGrouped, kKG>(t, args, pair_unit_ids<kGrouped>(t, args, lane));
+      const PairUnit& u = su.u;
       for (int slot = 0; slot < u.nslots; ++slot) {
       const PairSlot ps = pair_slot<kGrouped>(u, slot, args);
       const bool mine = ((ps.keep >> rank) & 1) != 0;
@@ -879,8 +929,8 @@ __global__ void __launch_bounds__(NatCfg<kBNs>::kThreads, 1)
         }
         ++xl;
       } else {
-        store_tile_rows<64, NC::kBoxes>(acc, tmap_c, args, out_box, row0, u.nb * kBNs + part * 64, lane,
-                                        stores_issued);
+        store_tile_rows<64, NC::kBoxes, kKG>(acc, tmap_c, args, out_box, row0, u.nb * kBNs + part * 64, lane,
+                                              stores_issued, su.gout);
       }
       }
     }
@@ -953,14 +1003,22 @@ PairKind pair_kind_t(bool scaled, bool wide) {
 }
 // variant = scaled + 2 * requant + 4 * NT layout + 8 * M-grouped (always NT)
 //           + 16 * 256-column block-scaled tiles (bf16 output, NT);
-// kKGroupedVariant: the FP32-promotion kernel over K ranges (bf16 output).
+// kKGroupedVariant: the FP32-promotion kernel over K ranges (bf16 output);
+// kKGroupedScaledVariant: the block-scaled kernel over K ranges.
 constexpr int kKGroupedVariant = 32;
-constexpr int kNumVariants = 33;
+constexpr int kKGroupedScaledVariant = 33;
+constexpr int kNumVariants = 34;
 PairKind pair_kind(int variant) {
   if (variant == kKGroupedVariant) {
     using C = PCfg<kEpiCols, false>;
     return {reinterpret_cast<const void*>(&fp8_gemm_pair_kernel<kEpiCols, false, false, true>), C::kThreads,
             C::kOutBytes + (2 * kMaxStages + 2 * kNumBuf + 1) * sizeof(uint64_t) + 16, kStageBytes, kMaxStages, 1};
+  }
+  if (variant == kKGroupedScaledVariant) {
+    using NC = NatCfg<128>;
+    return {reinterpret_cast<const void*>(&fp8_gemm_pair_scaled_kernel<false, false, false, 128, true>),
+            NC::kThreads, nat_out_bytes<128>(false) + (2 * kNatMaxStages + 4 + 1) * sizeof(uint64_t) + 16,
+            NC::kStageBytes, kNatMaxStages, NC::kKbPerStage};
   }
   const bool scaled = (variant & 1) != 0, wide = (variant & 16) != 0;
   if (variant & 8)
@@ -1204,8 +1262,11 @@ int launch_gemm_pair(const GemmProblem& p, cudaStream_t stream) {
 }
 
 int launch_gemm_pair_k_grouped(const GemmProblem& p, const int64_t* k_sizes, int num_groups, cudaStream_t stream) {
-  if (p.pow2_scales || p.rq.q || p.m_indices || p.sa_per_row || !p.a_mn || !p.b_mn || p.M <= kBM)
-    return DG_ERR_UNSUPPORTED_SHAPE;
+  if (p.rq.q || p.m_indices || p.sa_per_row || !p.a_mn || !p.b_mn || p.M <= kBM) return DG_ERR_UNSUPPORTED_SHAPE;
+  // Power-of-two scales: the block-scaled kernel (accumulators stay in TMEM
+  // across each range's K blocks); FP32 scales: the promotion kernel.
+  const bool scaled = p.pow2_scales;
+  const int variant = scaled ? kKGroupedScaledVariant : kKGroupedVariant;
   PairArgsKG args{};
   int nkg = 0;
   int64_t kb = 0, max_k = 0;
@@ -1237,58 +1298,63 @@ int launch_gemm_pair_k_grouped(const GemmProblem& p, const int64_t* k_sizes, int
   args.ld_sb = static_cast<int>(p.ld_sb);
   args.a_mn = 1;
   args.b_mn = 1;
-  args.idesc = kIdesc | idesc_majors(true, true);
+  args.idesc = (scaled ? NatCfg<128>::kIdesc : kIdesc) | idesc_majors(true, true);
   args.num_mb = static_cast<int>((p.M + kBM - 1) / kBM);
   args.num_pm = static_cast<int>((p.M + 2 * kBM - 1) / (2 * kBM));
   args.num_nb = static_cast<int>((p.N + kBN - 1) / kBN);
   args.group_pm = (p.M * max_k <= kRasterABytes) ? std::max(args.num_pm, 1) : kGroupPM;
   args.wait_limit_ns = kDefaultWaitLimitNs;
 
-  const PairKind kind = pair_kind(kKGroupedVariant);
+  const PairKind kind = pair_kind(variant);
   const size_t budget = kMaxDynSmem - 1024 - kind.fixed_smem;
   int stages = std::min<int>(kind.max_stages, static_cast<int>(budget / kind.stage_bytes));
   stages = stages / 2 * 2;
   if (stages < 4) return DG_ERR_UNSUPPORTED_SHAPE;
   args.num_stages = stages;
   const size_t smem = 1024 + static_cast<size_t>(stages) * kind.stage_bytes + kind.fixed_smem;
-  if (!set_pair_smem_attribute(kKGroupedVariant)) return DG_ERR_CUDA;
+  if (!set_pair_smem_attribute(variant)) return DG_ERR_CUDA;
   const int64_t units = static_cast<int64_t>(args.num_pm) * args.num_nb * nkg;
-  int pairs = max_active_pairs(kKGroupedVariant, smem);
+  int pairs = max_active_pairs(variant, smem);
   if (pairs <= 0) return DG_ERR_UNSUPPORTED_SHAPE;
   if (p.num_sms_cap > 0) pairs = std::min(pairs, p.num_sms_cap / 2);
   pairs = static_cast<int>(std::min<int64_t>(pairs, units));
   if (pairs < 1) return DG_ERR_UNSUPPORTED_SHAPE;
 
   CUtensorMap ta, tb, tc;
+  const uint32_t kbs = static_cast<uint32_t>(kind.kb_per_stage);
   {
-    // A as [K_tot][ld_a]: 128 (M) x 128 (K) boxes, 128-byte swizzle.
+    // A as [K_tot][ld_a]: 128 (M) x 128 kb_per_stage (K) boxes, 128-byte swizzle.
     const uint64_t dims[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(kb * kBK)};
     const uint64_t str[1] = {static_cast<uint64_t>(p.ld_a)};
-    const uint32_t box[2] = {kBM, kBK};
+    const uint32_t box[2] = {kBM, kBK * kbs};
     if (!encode_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a, 2, dims, str, box, true)) return DG_ERR_CUDA;
   }
   {
-    // B as [K_tot][ld_b]: 64 (N) x 128 (K) boxes, 64-byte swizzle.
+    // B as [K_tot][ld_b]: 64 (N) x 128 kb_per_stage (K) boxes, 64-byte swizzle.
     const uint64_t dims[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(kb * kBK)};
     const uint64_t str[1] = {static_cast<uint64_t>(p.ld_b)};
-    const uint32_t box[2] = {kBN / 2, kBK};
+    const uint32_t box[2] = {kBN / 2, kBK * kbs};
     if (!encode_tensor_map_swizzle(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, str, box,
                                    CU_TENSOR_MAP_SWIZZLE_64B))
       return DG_ERR_CUDA;
   }
   {
-    // C as bf16 [G][M][ld_c]: 32 x 32 x 1 boxes, 64-byte swizzle; rows past M
-    // of one matrix are clipped instead of reaching the next.
+    // C as bf16 [G][M][ld_c]: 64 x 32 x 1 boxes, 128-byte swizzle (the
+    // block-scaled kernel: 32 x 32 x 1, 64-byte swizzle); rows past M of one
+    // matrix are clipped instead of reaching the next.
     const uint64_t dims[3] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.M),
                               static_cast<uint64_t>(num_groups)};
     const uint64_t str[2] = {static_cast<uint64_t>(p.ld_c) * 2, static_cast<uint64_t>(p.ld_c) * 2 * p.M};
-    const uint32_t box[3] = {64, 32, 1};
+    const uint32_t box[3] = {scaled ? 32u : 64u, 32, 1};
     if (!encode_tensor_map_swizzle(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.c, 3, dims, str, box,
-                                   CU_TENSOR_MAP_SWIZZLE_128B))
+                                   scaled ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
       return DG_ERR_CUDA;
   }
-  const cudaError_t e = launch_kernel(fp8_gemm_pair_kernel<kEpiCols, false, false, true>, dim3(2 * pairs),
-                                      dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args);
+  const cudaError_t e =
+      scaled ? launch_kernel(fp8_gemm_pair_scaled_kernel<false, false, false, 128, true>, dim3(2 * pairs),
+                             dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args)
+             : launch_kernel(fp8_gemm_pair_kernel<kEpiCols, false, false, true>, dim3(2 * pairs),
+                             dim3(kind.threads), smem, stream, 2u, ta, tb, tc, args);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;

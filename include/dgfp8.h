@@ -282,10 +282,11 @@ DG_API int dg_fp8_gemm_requant(uint8_t *cq, int64_t ld_cq, float *cs, int out_bl
  *   k_sizes  HOST array of num_groups sizes, each >= 0 and a multiple of 128
  *            (DG_ERR_UNSUPPORTED_SHAPE otherwise); K_tot is their sum. A group
  *            of size 0 gets C_g = 0.
- * Alignment rules as dg_fp8_gemm_nt. With FP32 scales and M > 128 every
- * non-empty group runs in one launch on CTA pairs (at most 256 non-empty
- * groups; more take the per-group path); otherwise the groups run one after
- * another on `stream`. */
+ * Alignment rules as dg_fp8_gemm_nt. With M > 128 every non-empty group runs
+ * in one launch on CTA pairs (at most 256 non-empty groups; more take the
+ * per-group path): FP32 scales on the promotion kernel, power-of-two scales on
+ * the block-scaled one. Otherwise the groups run one after another on
+ * `stream`. */
 DG_API int dg_fp8_k_grouped_gemm_tn(void *c, int64_t ld_c,
                                     const uint8_t *a, int64_t ld_a, const float *sa,
                                     const uint8_t *b, int64_t ld_b, const float *sb,

@@ -167,19 +167,23 @@ def test_k_grouped_small_m_exact(oracle_mod):
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
-def test_k_grouped_many_ranges_exact(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_k_grouped_many_ranges_exact(oracle_mod, mode):
     """Twenty ranges of 0-384 rows (empty ones among them) in one launch: the
     units of consecutive ranges share the pairs, and a pair row (M = 384) and a
-    column tile (N = 320) cross the matrix edges of every output."""
+    column tile (N = 320) cross the matrix edges of every output. With
+    power-of-two scales, ranges of one and three K blocks end on a half-filled
+    two-block stage of the block-scaled kernel."""
     rng = np.random.default_rng(7)
     sizes = [int(v) * 128 for v in rng.integers(0, 4, 20)]
     sizes[0], sizes[-1] = 0, 256
-    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 384, 320, sizes, exact=True, seed=37)
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 384, 320, sizes, exact=True, seed=37, mode=mode)
     ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
-def test_k_grouped_padded_output_rows_untouched(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_k_grouped_padded_output_rows_untouched(oracle_mod, mode):
     """One launch writing C [G][M][ld_c] with ld_c > N: every value of the
     padding columns stays as it was (the 3-D output map clips at N and at M)."""
     sizes = [256, 0, 128, 384]
@@ -190,7 +194,8 @@ def test_k_grouped_padded_output_rows_untouched(oracle_mod):
     dev = device()
     c_full = torch.full((len(sizes), m, ld), float("nan"), dtype=torch.bfloat16, device=dev)
     c = c_full[:, :, :n]
-    bq.dg_fp8_k_grouped_gemm_tn(c, _padded(a_st, dev), _padded(b_st, dev), to_dev(sa, dev), to_dev(sb, dev), sizes)
+    bq.dg_fp8_k_grouped_gemm_tn(c, _padded(a_st, dev), _padded(b_st, dev), to_dev(sa, dev), to_dev(sb, dev), sizes,
+                                mode)
     assert bq.dg_get_device_status() == bq.DG_OK
     ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
@@ -207,14 +212,15 @@ def test_k_grouped_more_ranges_than_one_launch_holds_exact(oracle_mod):
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
-def test_k_grouped_moe_weight_gradient_sampled(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_k_grouped_moe_weight_gradient_sampled(oracle_mod, mode):
     """8 experts, token counts padded to 128 (the MoE layout's group sizes),
     M = 2048 hidden x N = 1408 intermediate: the shape of a weight gradient."""
     mo = synthetic.MOE
     sizes = synthetic.moe_group_sizes(mo["experts"], 2048, 2, 1)
     sizes = [int(-(-s // 128) * 128) for s in sizes]
     m, n = 2048, 1408
-    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, m, n, sizes, exact=False, seed=35)
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, m, n, sizes, exact=False, seed=35, mode=mode)
     rows = sample_rows(m, 16, seed=3)
     ref, mag = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes, rows=rows)
     idx = torch.as_tensor(rows, device=c.device)
