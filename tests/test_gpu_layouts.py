@@ -202,12 +202,13 @@ def test_k_grouped_padded_output_rows_untouched(oracle_mod, mode):
     assert torch.isnan(c_full[:, :, n:].float()).all()
 
 
-def test_k_grouped_more_ranges_than_one_launch_holds_exact(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_k_grouped_more_ranges_than_one_launch_holds_exact(oracle_mod, mode):
     """300 non-empty ranges: past the 256 a single launch carries, the ranges
     run one after another."""
     sizes = [128] * 300
     sizes[5] = 0
-    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 256, 128, sizes, exact=True, seed=39)
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 256, 128, sizes, exact=True, seed=39, mode=mode)
     ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
