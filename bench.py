@@ -427,6 +427,11 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 def _time_each(stream, fns, iters, warmup):
+    """Per-launch device time (median per function) with CUDA events around
+    each launch. A spin kernel first holds the stream for ~25 ms, so that the
+    host has queued every launch (and its events) before the device reaches
+    the first one: host-side argument marshalling never lands between an
+    event and its kernel."""
     import torch
     for _ in range(warmup):
         for f in fns:
@@ -434,6 +439,8 @@ def _time_each(stream, fns, iters, warmup):
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
            for _ in range(iters * len(fns))]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)
     k = 0
     for _ in range(iters):
         for f in fns:
