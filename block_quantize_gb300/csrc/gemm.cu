@@ -826,6 +826,16 @@ int launch_gemm(const GemmProblem& p, cudaStream_t stream) {
   if (sms <= 0) return DG_ERR_NO_DEVICE;
   // Decode shapes: one row streams B (gemv.cu); M <= 128, cluster split-K.
   if (!block_n_override() && gemv_supported(p)) return launch_gemv(p, stream);
+  // Small problems with 64-128 rows (B up to 12 MB, bf16 output, K-major B):
+  // one CTA per narrow tile over all of K starts faster than a cluster that
+  // splits K and reduces (single launches on GB300: 128x256x512 8.1 against
+  // 13.2 us, 128x2048x2048 12.7 against 18.3 us; at 16 rows, or from 16 MB of
+  // B, the split kernel is as fast or faster).
+  if (!block_n_override() && p.m_indices == nullptr && p.M >= 64 && p.M <= kBM && !p.rq.q && !p.b_mn &&
+      p.N * p.K <= (12ll << 20)) {
+    if ((p.N + 31) / 32 <= sms) return run_gemm<32, false, false>(p, stream, dev, sms);
+    return run_gemm<64, false, false>(p, stream, dev, sms);
+  }
   if (!block_n_override() && small_m_supported(p.M, p.m_indices)) return launch_gemm_small_m(p, stream);
   // Dense M > 128 and M-grouped calls with power-of-two scales: CTA pairs (the
   // grouped calls fall back to the 1-SM kernel below when fewer than two SMs
