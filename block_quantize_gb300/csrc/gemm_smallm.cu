@@ -776,7 +776,12 @@ int plan_and_run(const GemmProblem& p, cudaStream_t stream, int sms, const Small
         return run_small_m<192, kQ>(p, stream, a192, s192, p192);
     }
   }
-  if (ok256 && (!ok128 || p256.cost <= p128.cost)) return run_small_m<256, kQ>(p, stream, a256, s256, p256);
+  // Requantized output takes 128-column tiles whenever they fit: the 256-column
+  // requantizing kernel (19 warps, 96 registers a thread) spills in its tile
+  // tail, which the model does not see (128x24576x1536: 54.9 -> 33.0 us; the
+  // other decode shapes within 1 %).
+  if (ok256 && !(kQ && ok128) && (!ok128 || p256.cost <= p128.cost))
+    return run_small_m<256, kQ>(p, stream, a256, s256, p256);
   if (ok128) return run_small_m<128, kQ>(p, stream, a128, s128, p128);
   return DG_ERR_UNSUPPORTED_SHAPE;
 }
