@@ -130,6 +130,24 @@ def test_decode_192_column_tiles_with_ragged_last_tile(oracle_mod, m):
     assert_within_bound(c, ref, mag, f"{m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (64, 4096, 3072),    # 64 rows, B exactly 12 MiB: the 1-SM kernel, 32-column tiles (128 tiles)
+    (96, 7000, 1536),    # ragged N past one wave of 32-column tiles: 64-column tiles, last one cut
+    (128, 300, 640),     # ragged N inside one tile
+    (63, 1024, 1024),    # 63 rows: the split-K cluster kernel
+    (64, 8192, 2048),    # 16 MiB of B: the split-K cluster kernel
+])
+def test_small_problem_routing_edges(oracle_mod, m, n, k):
+    """Small GEMMs on both sides of the switch between the 1-SM kernel and the
+    split-K cluster kernel (64-128 rows, B up to 12 MiB), with ld_c > N so that
+    no store may cross N."""
+    qa, sa, qb, sb = _operands(oracle_mod, m, n, k, seed=2000 + m + n)
+    c, cbuf = _run(qa, sa, qb, sb, ldc_pad=24)
+    assert torch.isnan(cbuf[:, n:].float()).all()
+    ref, mag = oracle_mod.gemm_nt(qa, sa, qb, sb)
+    assert_within_bound(c, ref, mag, f"{m}x{n}x{k}")
+
+
 @pytest.mark.parametrize("size", synthetic.SQUARES)
 @pytest.mark.parametrize("mode", [0, 1])
 def test_square_shapes(oracle_mod, size, mode):
