@@ -467,7 +467,11 @@ __global__ void __launch_bounds__(PCfg<EC, kQ>::kThreads, 1)
 //   * warps 8 on: per tile, read the accumulator, release it, round to bf16
 //     and store.
 // A stage past an odd number of K blocks holds a zero-filled K block that gets
-// no MMA and no scale.
+// no MMA and no scale. K-grouped calls (kKG) give each unit its own K range:
+// its stages start at the range's first K block, a last stage past an odd
+// count holds the next range's first K block (again no MMA, no scale), and a
+// one-stage unit's issuer commits the accumulator twice, once for each
+// issuer the barrier counts.
 //
 // Two tile widths. 256x128 pair tiles (N = 128 MMAs, two accumulators of 128
 // columns alternating between tiles) serve every layout and the requantizing
