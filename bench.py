@@ -212,8 +212,8 @@ def run_reference(args):
 # DRAM bytes (read + write) per GEMM launch of the step, averaged over its four
 # shapes: one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, caches
 # flushed before each launch) of fp8_gemm_pair_kernel<64, 0, 1, 0> on GB300. Per
-# shape: 26.1, 44.9, 186.1, 82.8 MB. Measured again whenever that kernel changes.
-GEMM_DRAM_BYTES_PER_LAUNCH = (26086912 + 44926208 + 186127360 + 82818816) / 4
+# shape: 25.8, 44.9, 186.0, 83.0 MB. Measured again whenever that kernel changes.
+GEMM_DRAM_BYTES_PER_LAUNCH = (25824768 + 44923392 + 186037760 + 82969088) / 4
 
 
 def run_ours(args):
