@@ -160,9 +160,10 @@ def test_k_grouped_exact(oracle_mod, mode):
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
 
-def test_k_grouped_small_m_exact(oracle_mod):
+@pytest.mark.parametrize("mode", [0, 1])
+def test_k_grouped_small_m_exact(oracle_mod, mode):
     sizes = [128, 512]
-    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 96, 640, sizes, exact=True, seed=33)
+    c, (a_st, sa, b_st, sb) = _k_grouped(oracle_mod, 96, 640, sizes, exact=True, seed=33, mode=mode)
     ref, _ = oracle_mod.k_grouped_gemm_tn(a_st, sa, b_st, sb, sizes)
     assert torch.equal(_bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32)))
 
