@@ -52,13 +52,16 @@ constexpr size_t kMinSmemPerCta = 120 * 1024;
 constexpr int kMaxSplit = 8;
 constexpr int kMaxSplitC = kMaxSplit;
 
-template <int BN>
+template <int BN, bool kQ = false>
 struct SCfg {
-  // TMEM: 512 columns of buffers, one buffer per issuer (each issuer owns the
-  // buffer and the stages congruent to its index, so every mbarrier has one
-  // in-order waiter).
+  // TMEM: 512 columns of buffers. Issuer i owns the buffers and the stages
+  // congruent to i modulo the issuer count, so every mbarrier has one
+  // in-order waiter.
   static constexpr int kNumPBuf = 512 / BN;
-  static constexpr int kIssuers = kNumPBuf;
+  // The requantizing 128-column kernel takes two issuers (two buffers each):
+  // with 13 warps the compiler holds every thread to 128 registers, and the
+  // tile-end code spilled; 11 warps give it 168 (16x7168x16384: 39.2 -> 29.9 us).
+  static constexpr int kIssuers = (kQ && BN == 128) ? 2 : kNumPBuf;
   static constexpr int kFirstEpiWarp = 1 + kIssuers;
   static constexpr int kGroups = BN / 64;           // 64-column groups per tile
   static constexpr int kEpiWarps = 4 * kGroups;     // x 4 lane quadrants
@@ -155,7 +158,7 @@ __device__ __forceinline__ bool requant_cluster_tile(const SmallArgsQ& args, con
                                                      uint32_t* rq_xmax, uint64_t* rq_bar, uint64_t* consumed_bar,
                                                      volatile int* abort_flag, unsigned int* status,
                                                      uint64_t limit) {
-  using C = SCfg<BN>;
+  using C = SCfg<BN, true>;
   constexpr int kNB = C::kNBlk;
   constexpr int kT = C::kEpiWarps * 32;
   const RequantOut& o = args.rq;
@@ -254,10 +257,10 @@ __device__ __forceinline__ bool requant_cluster_tile(const SmallArgsQ& args, con
 }
 
 template <int BN, bool kQ>
-__global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
+__global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
     fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a,
                            const __grid_constant__ CUtensorMap tmap_b, const SmallArgsT<kQ> args) {
-  using C = SCfg<BN>;
+  using C = SCfg<BN, kQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -435,9 +438,9 @@ __global__ void __launch_bounds__(SCfg<BN>::kThreads, 1)
       // Tiles of up to 192 columns fetch the K blocks' scales three blocks
       // ahead: loaded in the block that uses them, their L2 latency paced every
       // block's promotion (16x24576x1536: 10.4 -> 9.5 us). The 256-column kernel
-      // (96 registers a thread) and the requantizing ones spilled more with the
-      // extra registers and ran slower: they keep the in-block load.
-      constexpr bool kPf = BN < 256 && !kQ;
+      // (96 registers a thread) spilled more with the extra registers and its
+      // blocks are long enough to hide the load: it keeps the in-block load.
+      constexpr bool kPf = BN < 256;
       const float* sa_p = args.sa + sa_off;
       float a0 = kPf && valid ? __ldg(sa_p + kb_lo) : 0.f, b0 = kPf && valid ? __ldg(sb_row + kb_lo) : 0.f;
       float a1 = kPf && valid && kb_lo + 1 < kb_hi ? __ldg(sa_p + kb_lo + 1) : 0.f;
@@ -610,7 +613,7 @@ int max_active_clusters(int split, size_t smem) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(split * 256, 1, 1);
-  cfg.blockDim = dim3(SCfg<BN>::kThreads, 1, 1);
+  cfg.blockDim = dim3(SCfg<BN, kQ>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -635,7 +638,7 @@ struct Plan {
 // with the least modelled time. Returns false if BN does not fit.
 template <int BN, bool kQ>
 bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_out, Plan& plan) {
-  using C = SCfg<BN>;
+  using C = SCfg<BN, kQ>;
   args.num_nb = static_cast<int>((p.N + BN - 1) / BN);
   const uint32_t stage_bytes = args.a_stage_bytes + C::kBTileBytes;
   const size_t bar_bytes = (2 * kMaxStages + 2 * C::kNumPBuf + 3) * sizeof(uint64_t) + 32;
@@ -755,11 +758,11 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
     if (!encode_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, p.b, 2, dims, strides, box, true))
       return DG_ERR_CUDA;
   }
-  args.idesc = SCfg<BN>::kIdesc | idesc_majors(p.a_mn, p.b_mn);
+  args.idesc = SCfg<BN, kQ>::kIdesc | idesc_majors(p.a_mn, p.b_mn);
   SmallArgsT<kQ> kargs;
   static_cast<SmallArgs&>(kargs) = args;
   if constexpr (kQ) kargs.rq = p.rq;
-  if (launch_kernel(fp8_gemm_splitk_kernel<BN, kQ>, dim3(args.split * args.num_clusters), dim3(SCfg<BN>::kThreads),
+  if (launch_kernel(fp8_gemm_splitk_kernel<BN, kQ>, dim3(args.split * args.num_clusters), dim3(SCfg<BN, kQ>::kThreads),
                     smem, stream, static_cast<unsigned>(args.split), ta, tb, kargs) != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
