@@ -13,11 +13,12 @@
 //     at ~4.8 TB/s with 128-row boxes and ~5.4 TB/s with 256-row boxes
 //     (measured on GB300), hence wide tiles and a split of K over the SMs;
 //   * the cluster then reduces its `split` FP32 partial tiles through
-//     distributed shared memory: every CTA parks its partial in its own shared
-//     memory and signals every peer's `ready` mbarrier; CTA r sums the peers'
-//     values for its share of the columns in rank order (deterministic), rounds
-//     to bf16 and stores; then it signals every peer's `consumed` mbarrier so
-//     the partial buffers can be reused for the next tile;
+//     distributed shared memory: CTA r owns a share of the tile's columns;
+//     every CTA stores each column unit of its partial into slot `rank` of
+//     the owner's buffer (remote stores) and signals every peer's `ready`
+//     mbarrier; CTA r sums the slots of its share in rank order
+//     (deterministic), rounds to bf16 and stores; then it signals every peer's
+//     `consumed` mbarrier so the buffers can be refilled for the next tile;
 //   * clusters are persistent over the N tiles.
 // All waits are bounded (see dg_device.cuh). The only unbounded synchronisation
 // is the cluster-wide barrier at kernel start (peers' barriers initialised
@@ -67,7 +68,7 @@ struct SCfg {
   static constexpr int kEpiWarps = 4 * kGroups;     // x 4 lane quadrants
   static constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
   static constexpr uint32_t kBTileBytes = BN * kBK;
-  static constexpr int kPartStride = BN + 4;        // +16 B: conflict-free row writes
+  static constexpr int kUnits = BN / 8;             // 8-column units of a tile (column shares)
   // Columns per tcgen05.ld: 16 when 19 warps leave 96 registers per thread.
   static constexpr int kChunk = (kThreads > 512) ? 16 : 32;
   static constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
@@ -98,7 +99,7 @@ struct SmallArgs {
   int split;          // cluster size = number of K ranges
   int num_clusters;   // persistent clusters (grid = num_clusters * split)
   int num_stages;
-  int m_pad;          // partial rows kept (multiple of 32, >= M)
+  int part_stride;    // floats per row of a reduction slot (split >= 2)
   uint32_t a_stage_bytes, a_box_bytes;
   uint64_t wait_limit_ns;
 };
@@ -111,6 +112,23 @@ struct SmallArgsQ : SmallArgs {
 };
 template <bool kQ>
 using SmallArgsT = std::conditional_t<kQ, SmallArgsQ, SmallArgs>;
+
+// Column shares of a cluster of `split` CTAs over a tile of `units` 8-column
+// units: rank r reduces and stores units [floor(r units / split),
+// floor((r + 1) units / split)).
+__host__ __device__ constexpr int share_lo(int r, int units, int split) { return r * units / split; }
+// Rank whose share holds unit u: the largest r with share_lo(r) <= u.
+__host__ __device__ constexpr int share_owner(int u, int units, int split) {
+  return ((u + 1) * split + units - 1) / units - 1;
+}
+// Widest share, in columns.
+__host__ __device__ constexpr int share_cols_max(int units, int split) { return (units + split - 1) / split * 8; }
+
+__device__ __forceinline__ void st_dsmem_f4(uint32_t cluster_addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
 
 // Eight consecutive outputs at column gcol as bf16 (a 16-byte store when all
 // eight are inside the matrix, else element by element up to N).
@@ -136,10 +154,10 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, int gcol, int N
 
 // Requantizing end of a tile for a cluster of split >= 2 CTAs. This CTA has
 // the sums of its column share; the block maxima span the cluster:
-//   1. sum this thread's items (row, 8 columns) over the peers' partials in
-//      rank order and keep them in registers (at most 4 items: work <=
-//      M * ceil(BN/8/split) <= 8 BN items over 2 BN threads), then release the
-//      peers' partial buffers (`consumed`);
+//   1. sum this thread's items (row, 8 columns) over the ranks' slots of this
+//      CTA's buffer in rank order and keep them in registers (at most 4 items:
+//      work <= M * ceil(BN/8/split) <= 8 BN items over 2 BN threads), then
+//      tell every peer that the buffer is read (`consumed`);
 //   2. fold each item's max|v| into this CTA's maxima (shared atomicMax on the
 //      bit patterns of non-negative floats), per (row, 128-column block) or
 //      per block; wait until every epilogue warp of the CTA has folded;
@@ -181,10 +199,10 @@ __device__ __forceinline__ bool requant_cluster_tile(const SmallArgsQ& args, con
       col[i] = col_lo + (g % groups8) * 8;
 #pragma unroll
       for (int q = 0; q < 8; ++q) v[i][q] = 0.f;
-      const uint32_t local = smem_u32(part + rr[i] * C::kPartStride + col[i]);
+      const float* src = part + rr[i] * args.part_stride + (col[i] - col_lo);
       for (int s = 0; s < split; ++s) {
-        const uint32_t ra = mapa_shared(local, s);
-        const float4 x0 = ld_dsmem_f4(ra), x1 = ld_dsmem_f4(ra + 16);
+        const float* q = src + s * args.M * args.part_stride;
+        const float4 x0 = *reinterpret_cast<const float4*>(q), x1 = *reinterpret_cast<const float4*>(q + 4);
         v[i][0] += x0.x; v[i][1] += x0.y; v[i][2] += x0.z; v[i][3] += x0.w;
         v[i][4] += x1.x; v[i][5] += x1.y; v[i][6] += x1.z; v[i][7] += x1.w;
       }
@@ -256,7 +274,10 @@ __device__ __forceinline__ bool requant_cluster_tile(const SmallArgsQ& args, con
   return true;
 }
 
-template <int BN, bool kQ>
+// kRed: the plan splits K (split >= 2) and the cluster reduces. The
+// instantiations without it carry no reduction code, which kept the compiler's
+// register allocation of their K loop as lean as before the reduction grew.
+template <int BN, bool kQ, bool kRed>
 __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
     fp8_gemm_splitk_kernel(const __grid_constant__ CUtensorMap tmap_a,
                            const __grid_constant__ CUtensorMap tmap_b, const SmallArgsT<kQ> args) {
@@ -273,7 +294,7 @@ __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
   // The partial tile parked for the cluster's reduction (split >= 2 only: a
   // CTA that reduces alone stores from registers and gets no buffer).
   float* part = reinterpret_cast<float*>(smem + off);
-  if (args.split > 1) off += static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float);
+  if constexpr (kRed) off += static_cast<size_t>(args.split) * args.M * args.part_stride * sizeof(float);
   // Requantized output (kQ): the block-max exchange.
   uint8_t* rq_xchg = nullptr;
   uint32_t* rq_pmax = nullptr;  // [2][128][kNBlk]
@@ -482,7 +503,7 @@ __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
       if (!ok) break;
 
       if constexpr (kQ) {
-        if (split == 1) {
+        if constexpr (!kRed) {
           // No peers: the epilogue slices exchange their maxima in this CTA.
           bool unused = false;
           if (!requant_store_slice<C::kEpiWarps>(acc, row < args.M, false, lg * 32, args.M, args.N, colt, ew, lane,
@@ -494,7 +515,7 @@ __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
           continue;
         }
       }
-      if (split == 1) {
+      if constexpr (!kRed) {
         // No peers: round this thread's row segment to bf16 and store it.
         if (row < args.M && valid) {
           __nv_bfloat16* dst = args.c + static_cast<int64_t>(row) * args.ld_c + colt;
@@ -508,22 +529,37 @@ __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
         continue;
       }
 
-      // Park this CTA's partial (rows < M) once every peer has read the last one.
+      // Push this CTA's partial (rows < M) to the ranks that reduce it, once
+      // every rank has read the last tile's: each 8-column unit goes into slot
+      // `rank` of its owner's buffer ([split][M][part_stride] floats, columns
+      // relative to the owner's share). Remote stores do not wait for a round
+      // trip the way remote loads of the peers' partials did.
       if (tile_seq > 0) {
         const bool w = mbar_wait_cluster(smem_u32(consumed_bar), (tile_seq - 1) & 1u, abort_flag, status, limit);
         ok = __all_sync(0xFFFFFFFFu, w);
         if (!ok) break;
       }
       if (row < args.M) {
-        float* prow = part + row * C::kPartStride + grp * 64;
+        const uint32_t slot_row = smem_u32(part + (static_cast<int>(rank) * args.M + row) * args.part_stride);
+        int owner = share_owner(grp * 8, C::kUnits, split);
+        int lo = share_lo(owner, C::kUnits, split), hi = share_lo(owner + 1, C::kUnits, split);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float2 lo = f32x2_split(acc[2 * j]), hi = f32x2_split(acc[2 * j + 1]);
-          reinterpret_cast<float4*>(prow)[j] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        for (int j = 0; j < 8; ++j) {
+          const int u = grp * 8 + j;
+          if (u >= hi) {  // next owner (shares are at least one unit wide)
+            ++owner;
+            lo = hi;
+            hi = share_lo(owner + 1, C::kUnits, split);
+          }
+          const uint32_t dst = mapa_shared(slot_row + (u - lo) * 32u, static_cast<uint32_t>(owner));
+          const float2 v0 = f32x2_split(acc[4 * j]), v1 = f32x2_split(acc[4 * j + 1]);
+          const float2 v2 = f32x2_split(acc[4 * j + 2]), v3 = f32x2_split(acc[4 * j + 3]);
+          st_dsmem_f4(dst, make_float4(v0.x, v0.y, v1.x, v1.y));
+          st_dsmem_f4(dst + 16, make_float4(v2.x, v2.y, v3.x, v3.y));
         }
       }
-      // The warp's writes are ordered (warp barrier) before the releasing remote
-      // arrives; lane s signals peer s, so the arrives to all peers overlap.
+      // The warp's stores are ordered (warp barrier) before the releasing remote
+      // arrives; lane s signals rank s, so the arrives to all ranks overlap.
       __syncwarp();
       if (lane < split) mbar_arrive_remote(mapa_shared(smem_u32(ready_bar), lane));
 
@@ -545,10 +581,10 @@ __global__ void __launch_bounds__(SCfg<BN, kQ>::kThreads, 1)
         float sum[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) sum[q] = 0.f;
-        const uint32_t local = smem_u32(part + rr * C::kPartStride + col);
+        const float* src = part + rr * args.part_stride + (col - col_lo);
         for (int s = 0; s < split; ++s) {
-          const uint32_t ra = mapa_shared(local, s);
-          const float4 x0 = ld_dsmem_f4(ra), x1 = ld_dsmem_f4(ra + 16);
+          const float* q = src + s * args.M * args.part_stride;
+          const float4 x0 = *reinterpret_cast<const float4*>(q), x1 = *reinterpret_cast<const float4*>(q + 4);
           sum[0] += x0.x; sum[1] += x0.y; sum[2] += x0.z; sum[3] += x0.w;
           sum[4] += x1.x; sum[5] += x1.y; sum[6] += x1.z; sum[7] += x1.w;
         }
@@ -618,7 +654,9 @@ int max_active_clusters(int split, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ>, &cfg) != cudaSuccess) {
+  const cudaError_t e = split > 1 ? cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ, true>, &cfg)
+                                   : cudaOccupancyMaxActiveClusters(&n, fp8_gemm_splitk_kernel<BN, kQ, false>, &cfg);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     n = -1;
   }
@@ -628,6 +666,7 @@ int max_active_clusters(int split, size_t smem) {
 
 struct Plan {
   int split = 0;
+  int part_stride = 0;
   int clusters = 0;
   int stages = 0;
   size_t smem = 0;
@@ -646,12 +685,13 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
     return std::max<size_t>(static_cast<size_t>(st) * stage_bytes,
                             static_cast<size_t>(st - 1) * args.a_stage_bytes + kATileBytes);
   };
-  // Stages and shared memory without (split = 1) and with (split >= 2) the
-  // parked partial tile: at M = 128 the partial takes ~100 KB, which a CTA
-  // that reduces alone spends on stages instead.
-  auto layout = [&](bool with_part, int& stages_out, size_t& smem_o) {
+  // Stages and shared memory for a K split: with split >= 2 each CTA holds
+  // the reduction buffer of its column share (split slots of M rows of the
+  // widest share; ~100 KB at M = 128), which a CTA that reduces alone spends
+  // on stages instead. `pst` is the slot row stride in floats.
+  auto layout = [&](int split, int pst, int& stages_out, size_t& smem_o) {
     const size_t part_bytes =
-        (with_part ? (static_cast<size_t>(args.m_pad) * C::kPartStride * sizeof(float) + 15) / 16 * 16 : 0) +
+        (split > 1 ? (static_cast<size_t>(split) * p.M * pst * sizeof(float) + 15) / 16 * 16 : 0) +
         (kQ ? C::kRqBytes : 0);
     if (part_bytes + bar_bytes + 1024 >= kMaxDynSmem) return false;
     const size_t budget = kMaxDynSmem - 1024 - part_bytes - bar_bytes;
@@ -666,10 +706,6 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
     smem_o = smem;
     return true;
   };
-  int stages1 = 0, stagesN = 0;
-  size_t smem1 = 0, smemN = 0;
-  const bool ok1 = layout(false, stages1, smem1), okN = layout(true, stagesN, smemN);
-  if (!ok1 && !okN) return false;
 
   // Model (measured on GB300 with TMA streams of 128-byte rows): one SM
   // streams ~45 GB/s; all SMs together ~4.8 TB/s with 128-row boxes and
@@ -681,8 +717,21 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
   const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (split > args.num_kb || (BN / 8) / split < 1) break;
-    if (!(split == 1 ? ok1 : okN)) continue;
-    const size_t smem = split == 1 ? smem1 : smemN;
+    // Slot rows padded by 16 bytes (conflict-free pushes), unpadded where the
+    // padding would cost stages.
+    const int widest = share_cols_max(C::kUnits, split);
+    int pst = widest + 4, stages = 0;
+    size_t smem = 0;
+    if (!layout(split, pst, stages, smem)) continue;
+    if (split > 1) {
+      int st0 = 0;
+      size_t sm0 = 0;
+      if (layout(split, widest, st0, sm0) && st0 > stages) {
+        pst = widest;
+        stages = st0;
+        smem = sm0;
+      }
+    }
     const int active = max_active_clusters<BN, kQ>(split, smem);
     if (active <= 0) continue;
     int clusters = std::min(active, args.num_nb);
@@ -697,7 +746,8 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
       plan.cost = cost;
       plan.split = split;
       plan.clusters = clusters;
-      plan.stages = split == 1 ? stages1 : stagesN;
+      plan.stages = stages;
+      plan.part_stride = pst;
       plan.smem = smem;
     }
   }
@@ -715,7 +765,9 @@ bool set_smem_attribute() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (attr_set.load() & (1ull << dev)) return true;
-  if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN, kQ, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kMaxDynSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(fp8_gemm_splitk_kernel<BN, kQ, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kMaxDynSmem)) != cudaSuccess) {
     cudaGetLastError();
     return false;
@@ -728,6 +780,7 @@ template <int BN, bool kQ>
 int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_t smem, const Plan& plan) {
   args.split = plan.split;
   args.num_clusters = plan.clusters;
+  args.part_stride = plan.part_stride;
   CUtensorMap ta, tb;
   const uint32_t a_rows = args.a_box_bytes / kBK;
   if (p.a_mn) {
@@ -762,8 +815,13 @@ int run_small_m(const GemmProblem& p, cudaStream_t stream, SmallArgs args, size_
   SmallArgsT<kQ> kargs;
   static_cast<SmallArgs&>(kargs) = args;
   if constexpr (kQ) kargs.rq = p.rq;
-  if (launch_kernel(fp8_gemm_splitk_kernel<BN, kQ>, dim3(args.split * args.num_clusters), dim3(SCfg<BN, kQ>::kThreads),
-                    smem, stream, static_cast<unsigned>(args.split), ta, tb, kargs) != cudaSuccess) {
+  const cudaError_t e =
+      args.split > 1
+          ? launch_kernel(fp8_gemm_splitk_kernel<BN, kQ, true>, dim3(args.split * args.num_clusters),
+                          dim3(SCfg<BN, kQ>::kThreads), smem, stream, static_cast<unsigned>(args.split), ta, tb, kargs)
+          : launch_kernel(fp8_gemm_splitk_kernel<BN, kQ, false>, dim3(args.num_clusters), dim3(SCfg<BN, kQ>::kThreads),
+                          smem, stream, 1u, ta, tb, kargs);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }
@@ -832,7 +890,6 @@ int launch_gemm_small_m(const GemmProblem& p, cudaStream_t stream) {
   args.b_mn = p.b_mn ? 1 : 0;
   args.nbs = static_cast<int>((p.N + kBK - 1) / kBK);
   args.wait_limit_ns = kDefaultWaitLimitNs;
-  args.m_pad = static_cast<int>((p.M + 31) / 32 * 32);
   // K-major A: the valid rows (a multiple of 8); MN-major A: a full 128-byte-wide box.
   const uint32_t a_rows = p.a_mn ? kBM : static_cast<uint32_t>((p.M + 7) / 8 * 8);
   args.a_box_bytes = a_rows * kBK;
