@@ -74,6 +74,24 @@ def test_exact_bit_identical(oracle_mod, shape, layout, mode):
     assert torch.equal(got, want), f"{int((got != want).sum())} outputs differ"
 
 
+# Decode shapes whose plans cover the cluster reduction's K splits 2, 4, 5, 6 and 8
+# (column shares of uneven width, pushed to their owners), a ragged last tile and
+# odd row counts, plus a plan without a K split.
+DECODE_SHAPES = [(16, 7168, 16384), (64, 7168, 16384), (128, 7168, 16384), (128, 2112, 7168), (16, 1536, 7168),
+                 (5, 4000, 2048), (77, 2000, 4096), (16, 24576, 1536)]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("shape", DECODE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_exact_decode_splits(oracle_mod, shape, mode):
+    m, n, k = shape
+    qa, sa, qb, sb = _exact_logical(m, n, k, seed=7 * m + n + k)
+    c = _run(qa, sa, qb, sb, m, n, "NT", mode)
+    ref, _ = oracle_mod.gemm_layout(qa, sa, qb, sb, "NT")
+    got, want = _bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32))
+    assert torch.equal(got, want), f"{int((got != want).sum())} outputs differ"
+
+
 @pytest.mark.parametrize("layout", ["TN", "NN", "TT"])
 def test_exact_one_sm_fallback(oracle_mod, layout):
     """One SM allowed: the 1-SM kernel (256-column tiles) with MN-major operands."""
