@@ -92,6 +92,24 @@ def test_exact_decode_splits(oracle_mod, shape, mode):
     assert torch.equal(got, want), f"{int((got != want).sum())} outputs differ"
 
 
+@pytest.mark.parametrize("cap", [4, 10])
+@pytest.mark.parametrize("shape", [(16, 7168, 4096), (77, 2000, 2048), (128, 4096, 2048)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_exact_decode_many_tiles_per_cluster(oracle_mod, shape, cap):
+    """An SM cap leaves a few clusters for many tiles: every cluster's
+    reduction buffers and barriers go through many phases (tile after tile)."""
+    m, n, k = shape
+    qa, sa, qb, sb = _exact_logical(m, n, k, seed=3 * m + cap)
+    try:
+        bq.dg_set_num_sms(cap)
+        c = _run(qa, sa, qb, sb, m, n, "NT", 0)
+    finally:
+        bq.dg_set_num_sms(0)
+    ref, _ = oracle_mod.gemm_layout(qa, sa, qb, sb, "NT")
+    got, want = _bf16_bits(c.float()), _bf16_bits(ref.astype(np.float32))
+    assert torch.equal(got, want), f"{int((got != want).sum())} outputs differ"
+
+
 @pytest.mark.parametrize("layout", ["TN", "NN", "TT"])
 def test_exact_one_sm_fallback(oracle_mod, layout):
     """One SM allowed: the 1-SM kernel (256-column tiles) with MN-major operands."""

@@ -78,6 +78,23 @@ def test_exact_decode_cluster(oracle_mod, shape, block_rows, out_mode):
     assert np.array_equal(q, qr), f"codes differ at {np.argwhere(q != qr)[:5].tolist()}"
 
 
+@pytest.mark.parametrize("cap", [4, 10])
+@pytest.mark.parametrize("shape", [(16, 7168, 4096), (77, 2000, 2048)], ids=lambda s: "x".join(map(str, s)))
+def test_exact_decode_many_tiles_per_cluster(oracle_mod, shape, cap):
+    """An SM cap leaves a few clusters for many tiles: every cluster's
+    reduction buffers and barriers go through many phases (tile after tile)."""
+    m, n, k = shape
+    qa, sa, qb, sb = _exact_operands(m, n, k, seed=5 * m + cap)
+    try:
+        bq.dg_set_num_sms(cap)
+        q, s = _run_dense(qa, sa, qb, sb, 0, 1, 0)
+    finally:
+        bq.dg_set_num_sms(0)
+    qr, sr, _, _ = oracle_mod.gemm_nt_requant(qa, sa, qb, sb, 1, 0)
+    assert np.array_equal(s, sr), f"scales differ at {np.argwhere(s != sr)[:5].tolist()}"
+    assert np.array_equal(q, qr), f"codes differ at {np.argwhere(q != qr)[:5].tolist()}"
+
+
 @pytest.mark.parametrize("block_rows", [1, 128])
 def test_random_decode_cluster(oracle_mod, block_rows):
     m, n, k = 128, 7168, 16384
