@@ -27,8 +27,8 @@ configs = the other workloads of the metric, each timed in a bounded region
           after the line's own: the quantizer on a 16384x7168 FP32 activation
           (GB/s), the decode GEMMs M in {1,16,64,128} x (N,K) in
           {(24576,1536),(7168,16384)} (GB/s, graph-replayed), the MoE grouped
-          GEMM of 8 experts (TFLOP/s) and the squares 4096^3 and 8192^3 with
-          FP32 and power-of-two scales (TFLOP/s), each with its fraction of the
+          GEMM of 8 experts (TFLOP/s) and the squares 4096^3, 8192^3 and
+          16384^3 with FP32 and power-of-two scales (TFLOP/s), each with its fraction of the
           roofline that bounds it. Memory-bound cases rotate input copies
           beyond L2.
 
@@ -612,7 +612,7 @@ def config_records(dev, gen, stream, fp8_peak, hbm):
     grouped = [grouped_record(dev, gen, stream, steps, warmup, fp8_peak, mode) for mode in (0, 1)]
     squares = []
     for mode in (0, 1):
-        squares += gemm_records(dev, gen, stream, [(s_, s_, s_) for s_ in synthetic.SQUARES[:2]], mode,
+        squares += gemm_records(dev, gen, stream, [(s_, s_, s_) for s_ in synthetic.SQUARES], mode,
                                 steps, warmup, fp8_peak)
     tiny = gemm_records(dev, gen, stream, [synthetic.TINY], 0, steps, warmup, fp8_peak)
     tiny[0]["bound"] = "latency"
