@@ -707,13 +707,15 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
     return true;
   };
 
-  // Model (measured on GB300 with TMA streams of 128-byte rows): one SM
-  // streams ~45 GB/s; all SMs together ~4.8 TB/s with 128-row boxes and
-  // ~5.4 TB/s with 256-row boxes; a cluster reduction costs ~1 us per tile
-  // (mostly waiting for the slowest peer; measured, then swept). Time = max(whole-GPU stream of B,
-  // the slowest cluster's K range per tile + its reductions).
+  // Model (fitted to graph-timed sweeps of forced plans on GB300): one SM
+  // streams ~45 GB/s of 128-byte TMA rows; the whole GPU streams B at ~4.4,
+  // 5.2 and 4.6 TB/s with 128-, 192- and 256-column tiles as the kernel runs
+  // them; A's rows (from L2) count half; a tile's cluster reduction adds
+  // ~0.25 us per CTA of the split after its stream (the wait for the slowest
+  // peer grows with the split). Time = max(whole-GPU stream of B, the slowest
+  // cluster's K ranges) + reductions.
   const double sm_bytes_per_us = 4.5e4;
-  const double gpu_bytes_per_us = (BN == 256) ? 5.4e6 : (BN == 192) ? 5.2e6 : 4.8e6;
+  const double gpu_bytes_per_us = (BN == 256) ? 4.6e6 : (BN == 192) ? 5.2e6 : 4.4e6;
   const double b_bytes = static_cast<double>(p.N) * static_cast<double>(p.K);
   for (int split = 1; split <= kMaxSplit; ++split) {
     if (split > args.num_kb || (BN / 8) / split < 1) break;
@@ -738,10 +740,15 @@ bool plan_small_m(const GemmProblem& p, int sms, SmallArgs& args, size_t& smem_o
     if (p.num_sms_cap > 0) clusters = std::min(clusters, std::max(1, p.num_sms_cap / split));
     if (clusters <= 0 || clusters * split > sms * 2) continue;
     const int waves = (args.num_nb + clusters - 1) / clusters;
+    // A K split serves to fill the GPU in one wave; split plans that need
+    // several ran 25-40 % slower than a smaller split in every sweep. (Under
+    // an SM cap every plan needs several waves; the model chooses.)
+    if (split > 1 && waves > 1 && p.num_sms_cap <= 0) continue;
     const int kbs = (args.num_kb + split - 1) / split;
     const double per_cluster =
-        waves * (kbs * static_cast<double>(C::kBTileBytes) / sm_bytes_per_us + (split > 1 ? 1.0 : 0.0));
-    const double cost = std::max(b_bytes / gpu_bytes_per_us, per_cluster) * (1.0 + 0.01 * split);
+        waves * kbs * (static_cast<double>(C::kBTileBytes) + 0.5 * args.a_box_bytes) / sm_bytes_per_us;
+    const double reduce = split > 1 ? waves * 0.25 * split : 0.0;
+    const double cost = (std::max(b_bytes / gpu_bytes_per_us, per_cluster) + reduce) * (1.0 + 0.01 * split);
     if (cost < plan.cost) {
       plan.cost = cost;
       plan.split = split;
